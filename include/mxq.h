@@ -1,0 +1,216 @@
+/*
+ * mxq.h — C ABI of libmxq: weight-quantized scaled GEMM and routed fused MoE
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * Conventions (all entry points):
+ *   - The caller owns all memory.  Tensor arguments are DEVICE pointers on the
+ *     current CUDA device unless stated otherwise.  Scratch comes from a
+ *     caller-provided device workspace sized by the matching *_workspace_size
+ *     query; the library never calls cudaMalloc/cudaFree.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and returns an mxq_status.
+ *   - Arguments are validated on the host before anything is launched; on an
+ *     error nothing is launched, outputs are untouched, and
+ *     mxq_last_error() (thread-local) describes the problem.
+ *   - Problems detected on the device (an expert id outside [0, E), a bounded
+ *     wait that expired) set a device status word that mxq_sync_status reads.
+ *   - The device must be compute capability 10.3 (GB300, sm_103a); any other
+ *     device gives MXQ_ERR_UNSUPPORTED.
+ *   - Row strides (ld*) are in elements.  Operands read by the tensor-memory
+ *     accelerator (A, W, hidden, expert weights) need a 16-byte aligned base
+ *     and a row stride that is a multiple of 16 bytes, else
+ *     MXQ_ERR_UNSUPPORTED.
+ *
+ * Page references are "title, section" of the pages this library follows:
+ *   [CPU-MoE]  vLLM PR 50949 "[CPU] routed FP8/MXFP4 MoE: per-expert-block
+ *              BRGEMM vs TinyGEMM dispatch"
+ *   [CPU-GEMM] SGLang PR 32618 "[CPU] fp8_per_tensor_scaled_mm_cpu"
+ *   [XPU-FP8]  SGLang PR 35605 "[XPU] block-FP8 linear via torch scaled_mm"
+ */
+#ifndef MXQ_H_
+#define MXQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t mxq_status;
+typedef void* mxq_stream_t; /* a cudaStream_t */
+
+enum {
+  MXQ_OK = 0,
+  MXQ_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad stride, ... */
+  MXQ_ERR_UNSUPPORTED = 2, /* wrong device, block size, dtype combination, alignment */
+  MXQ_ERR_CUDA = 3,        /* a CUDA runtime/driver call or launch failed */
+  MXQ_ERR_TIMEOUT = 4,     /* a bounded device wait expired (mxq_sync_status) */
+  MXQ_ERR_DEVICE = 5       /* device-detected bad input, e.g. expert id out of range */
+};
+
+/* dtype tags */
+enum {
+  MXQ_BF16 = 1,
+  MXQ_F32 = 2,
+  MXQ_E4M3 = 3,   /* float8_e4m3fn, one byte */
+  MXQ_E2M1X2 = 4, /* two FP4 e2m1 codes per byte, low nibble = even index */
+  MXQ_UE8M0 = 5   /* one byte, value 2^(e-127) */
+};
+
+/* expert weight formats of mxq_fused_experts */
+enum {
+  MXQ_W_FP8_BLOCK128 = 1, /* e4m3 weights, fp32 scale per [128, 128] block */
+  MXQ_W_MXFP4 = 2         /* e2m1x2 weights, ue8m0 scale per 32 K elements */
+};
+
+/* options (process-wide; mxq_set_option / mxq_get_option) */
+enum {
+  MXQ_OPT_SMALL_M_MAX = 1,  /* expert blocks with m_size <= this use the narrowest MMA
+                               instruction covering them; larger blocks use the full
+                               block_m width.  Default 1 << 30 (always fit). */
+  MXQ_OPT_FORCE_PATH = 2,   /* 0 auto, 1 always narrow (fit), 2 always full width */
+  MXQ_OPT_WAIT_BUDGET_NS = 3, /* limit of every device-side wait, default 2e9 ns */
+  MXQ_OPT_SPLIT_K = 4,      /* fp8_scaled_mm split-K: 0 auto, else the factor */
+  MXQ_OPT_INJECT_STALL = 5, /* TEST ONLY: GEMM producers issue no copy, so every
+                               consumer wait runs out (exercises MXQ_ERR_TIMEOUT) */
+  MXQ_OPT_NUM_SMS = 6       /* persistent grid size cap; 0 = all SMs */
+};
+
+const char* mxq_last_error(void);
+const char* mxq_version(void);
+mxq_status mxq_set_option(int32_t option, int64_t value);
+mxq_status mxq_get_option(int32_t option, int64_t* value);
+
+/* Synchronizes `stream`, then reads and clears the device status word of the
+ * current device: MXQ_OK, MXQ_ERR_TIMEOUT or MXQ_ERR_DEVICE. */
+mxq_status mxq_sync_status(mxq_stream_t stream);
+
+/*
+ * Per-token-group FP8 quantization of activations ([XPU-FP8], key code
+ * excerpts: per_token_group_quant_fp8(input_2d, block_k) producing the
+ * BlockWise1x128 activation operand and its [M, K/128] scale).
+ * For every row m and group g of `group` consecutive K elements:
+ *     s[m, g] = max(amax_g, eps) / 448          (fp32, IEEE division)
+ *     q[m, k] = e4m3_rne(clamp(x[m, k] / s, -448, 448))  (IEEE division)
+ *   x       bf16 [M, K], row stride ldx (>= K), inner stride 1
+ *   q       e4m3 [M, K], row stride K (written)
+ *   scales  fp32 [M, ceil(K/group)] row-major (written); a ragged last group
+ *           uses its own amax
+ *   group   multiple of 8, 8..1024 (the pages use 128); eps > 0
+ * M == 0 is a no-op.
+ */
+mxq_status mxq_per_token_group_quant_fp8(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                         int32_t group, float eps, void* q, float* scales,
+                                         mxq_stream_t stream);
+
+/*
+ * Scaled FP8 GEMM  out[m, n] = sum_k A[m, k] * W[n, k] * scales (+ bias[n]).
+ * W8A8 block mode ([XPU-FP8], torch_w8a8_block_fp8_linear excerpt):
+ *   a_dtype = MXQ_E4M3, a_scale fp32 [M, ceil(K/128)] (strides sa0, sa1),
+ *   w_scale fp32 [ceil(N/block_n), ceil(K/128)] (strides sw0, sw1, any
+ *   layout, e.g. the transposed-contiguous storage of the load-time relayout),
+ *   block_n in {1, 128}, block_k = 128:
+ *     out = sum_kb As[m,kb] * Ws[n/block_n, kb] * sum_{k in kb} qA[m,k] W[n,k]
+ * W8A16 per-tensor mode ([CPU-GEMM], implementation breakdown: the per-tensor
+ *   scale is the block-scale case with every block equal):
+ *   a_dtype = MXQ_BF16, a_scale = NULL, w_scale = one fp32 (0-d or [1]),
+ *   block_n = block_k = 0:   out = (A . W^T) * s
+ * W8A16 with block weights (a_dtype = MXQ_BF16, a_scale = NULL, block scales)
+ * and W8A8 with a per-tensor weight scale are also accepted.
+ *   A      [M, K] e4m3 or bf16, row stride lda
+ *   W      e4m3 [N, K], row stride ldw
+ *   bias   NULL, or [N] of bias_dtype MXQ_F32 / MXQ_BF16
+ *   out    [M, N] row stride ldo; out_dtype MXQ_BF16 (rounded to nearest even
+ *          from the fp32 accumulator) or MXQ_F32 (the accumulator itself)
+ *   workspace / ws_bytes: optional device scratch for split-K (see
+ *          mxq_fp8_scaled_mm_workspace_size); NULL/0 disables split-K.
+ * Block sizes other than [128,128], [1,128] and per-tensor (e.g. MXFP8
+ * [1, 32]) give MXQ_ERR_UNSUPPORTED, as the page's block_size check does.
+ * M == 0 or N == 0 is a no-op; K must be positive.
+ */
+mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t M, int64_t K, int64_t lda,
+                             const float* a_scale, int64_t sa0, int64_t sa1, const void* W,
+                             int64_t N, int64_t ldw, const float* w_scale, int32_t block_n,
+                             int32_t block_k, int64_t sw0, int64_t sw1, const void* bias,
+                             int32_t bias_dtype, void* out, int32_t out_dtype, int64_t ldo,
+                             void* workspace, size_t ws_bytes, mxq_stream_t stream);
+
+/* Workspace bytes that let mxq_fp8_scaled_mm use its preferred split-K plan
+ * for this shape on the current device (0 when no split is needed). */
+mxq_status mxq_fp8_scaled_mm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t a_dtype,
+                                            size_t* bytes);
+
+/*
+ * Expert-block alignment ([CPU-MoE], the stage-1 tile loop consumes
+ * sorted_ids / expert_ids / offsets: block mb holds expert expert_ids[mb];
+ * its token slots are sorted_ids[mb*block_m + m] for
+ * m < offsets[mb+1] - offsets[mb]; the token of a slot is slot / topk).
+ *   topk_ids   int32 [T, topk], values in [0, E)
+ *   sorted_ids int32 [cap * block_m]: slots sorted by expert (ascending),
+ *              stable (ascending slot) within an expert, each expert's slots
+ *              split into blocks of block_m; padding = S = T*topk
+ *   expert_ids int32 [cap]: expert of each block, -1 past num_blocks
+ *   offsets    int32 [cap + 1]: compact prefix sum of block sizes,
+ *              offsets[0] = 0, = S past num_blocks
+ *   num_blocks int32 [1]
+ *   cap        >= ceil(S/block_m) + min(E, S) (the bound on the block count)
+ * Limits: 1 <= E <= 1024, block_m in {16, 32, 64, 128}.  Ids outside [0, E)
+ * are skipped and flagged (MXQ_ERR_DEVICE from mxq_sync_status).
+ * workspace: none needed (pass NULL, 0).
+ */
+mxq_status mxq_moe_align_block(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
+                               int32_t block_m, int32_t* sorted_ids, int32_t* expert_ids,
+                               int32_t* offsets, int32_t* num_blocks, int64_t cap,
+                               void* workspace, size_t ws_bytes, mxq_stream_t stream);
+
+/*
+ * Routed fused MoE ([CPU-MoE], implementation breakdown: stage 1
+ * hidden @ w1 per expert block, the activation, stage 2 @ w2; followed by the
+ * top-k weighted combine).  For every slot (t, k), e = topk_ids[t, k]:
+ *     h   = hidden[t] . W1[e]^T (+ b1[e])            [2N], fp32
+ *     act = bf16( silu(h[:N]) * h[N:] )                [N]
+ *     z   = act . W2[e]^T (+ b2[e])                    [K], fp32
+ *   out[t] = bf16( sum_k topk_weights[t, k] * z_(t,k) ), ascending k.
+ * Activations stay bf16 (W8A16): weights are decoded exactly to bf16.
+ *   hidden   bf16 [T, K], row stride ldh
+ *   wtype MXQ_W_FP8_BLOCK128:
+ *     w1 e4m3 [E, 2N, K], w1_scale fp32 [E, ceil(2N/128), ceil(K/128)]
+ *     w2 e4m3 [E, K, N],  w2_scale fp32 [E, ceil(K/128), ceil(N/128)]
+ *   wtype MXQ_W_MXFP4 (K, N multiples of 32):
+ *     w1 e2m1x2 [E, 2N, K/2], w1_scale ue8m0 [E, 2N, K/32]
+ *     w2 e2m1x2 [E, K, N/2],  w2_scale ue8m0 [E, K, N/32]
+ *   w1_bias fp32 [E, 2N] or NULL; w2_bias fp32 [E, K] or NULL
+ *   topk_weights fp32 [T, topk]; topk_ids int32 [T, topk]
+ *   block_m  in {16, 32, 64, 128}: tokens per expert block
+ *   out      bf16 [T, K], row stride ldo
+ *   workspace: mxq_fused_experts_workspace_size bytes, 256-byte aligned
+ */
+mxq_status mxq_fused_experts(const void* hidden, int64_t T, int64_t K, int64_t ldh, int32_t wtype,
+                             int32_t E, int64_t N, const void* w1, const void* w1_scale,
+                             const float* w1_bias, const void* w2, const void* w2_scale,
+                             const float* w2_bias, const float* topk_weights,
+                             const int32_t* topk_ids, int32_t topk, int32_t block_m, void* out,
+                             int64_t ldo, void* workspace, size_t ws_bytes, mxq_stream_t stream);
+
+/* Same as mxq_fused_experts, and additionally copies the checkpoints in slot
+ * order (slot = t*topk + k): act_out bf16 [T*topk, N] and y_out fp32
+ * [T*topk, K] = topk_weight * z.  Either may be NULL. */
+mxq_status mxq_fused_experts_debug(const void* hidden, int64_t T, int64_t K, int64_t ldh,
+                                   int32_t wtype, int32_t E, int64_t N, const void* w1,
+                                   const void* w1_scale, const float* w1_bias, const void* w2,
+                                   const void* w2_scale, const float* w2_bias,
+                                   const float* topk_weights, const int32_t* topk_ids,
+                                   int32_t topk, int32_t block_m, void* out, int64_t ldo,
+                                   void* workspace, size_t ws_bytes, void* act_out,
+                                   float* y_out, mxq_stream_t stream);
+
+mxq_status mxq_fused_experts_workspace_size(int64_t T, int64_t K, int32_t E, int64_t N,
+                                            int32_t topk, int32_t block_m, int32_t wtype,
+                                            size_t* bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXQ_H_ */

@@ -1,0 +1,24 @@
+// gemm_dense.cu — instantiations of the scaled-GEMM kernel for
+// fp8_scaled_mm, and the launcher that dispatches every GEMM.
+#include "gemm_launch.cuh"
+
+namespace mxq {
+
+cudaError_t launch_gemm_moe(int kind, int epi, int bt, bool promote, const GemmMaps& maps,
+                            const GemmParams& p, int grid, cudaStream_t stream);
+
+cudaError_t launch_gemm(int kind, int epi, int bt, bool promote, const GemmMaps& maps,
+                        const GemmParams& p, int grid, cudaStream_t stream) {
+  if (epi != EPI_DENSE) return launch_gemm_moe(kind, epi, bt, promote, maps, p, grid, stream);
+  if (kind == KIND_F8F8) {
+    // activation group scales always present: every slice is promoted
+    return launch_gemm_bt<KIND_F8F8, EPI_DENSE, true>(bt, maps, p, grid, stream);
+  }
+  if (kind == KIND_F8W) {
+    return promote ? launch_gemm_bt<KIND_F8W, EPI_DENSE, true>(bt, maps, p, grid, stream)
+                   : launch_gemm_bt<KIND_F8W, EPI_DENSE, false>(bt, maps, p, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mxq

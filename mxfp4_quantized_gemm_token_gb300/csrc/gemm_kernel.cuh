@@ -1,0 +1,697 @@
+// gemm_kernel.cuh — the tcgen05 scaled-GEMM kernel behind fp8_scaled_mm and
+// both fused-MoE stages.
+//
+// Orientation ("swap-AB"): the weight matrix W [rows, K] is the MMA's M side
+// (128 rows per tile, one TMEM lane per weight row) and the tokens [tokens, K]
+// are the MMA's N side (BT columns).  Decode-size token counts then cost a
+// narrow instruction instead of a mostly-empty 128-row tile, and the same
+// code serves large token counts with BT = 128.
+//
+// Warp roles (one CTA per SM, persistent over work units):
+//   warp 0        TMA producer for the weight operand (A ring)
+//   warp 1        TMEM allocator + single-thread tcgen05.mma issuer
+//   warp 2        TMA producer for the token operand (B ring)
+//   warps 4..7    epilogue: TMEM -> registers, scale promotion, output
+//   warps 8..11   (bf16 kinds only) in-shared-memory weight decode
+//                 e4m3 -> bf16 or e2m1 x 2^(e-127) -> bf16
+//
+// Block scales ("[XPU] block-FP8 linear via torch scaled_mm": activations
+// BlockWise1x128, weights BlockWise128x128 or 1x128) are not powers of two, so
+// they cannot ride the hardware block-scaled MMA.  Instead each 128-wide K
+// slice is accumulated into its own TMEM buffer (two buffers, ping-pong) and
+// the epilogue folds it into fp32 registers with the slice's scale product:
+//   acc[n, m] += Ws(n, kb) * As(m, kb) * partial_kb[n, m]
+// which is the definition of the scaled product evaluated slice by slice.
+// Per-tensor W8A16 scaling and MXFP4 (exact bf16 decode) accumulate in TMEM
+// across all of K and scale once.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace mxq {
+
+enum { KIND_F8F8 = 0, KIND_F8W = 1, KIND_MXW = 2 };
+enum { EPI_DENSE = 0, EPI_SILU = 1, EPI_SCATTER = 2 };
+enum { DT_BF16 = 1, DT_F32 = 2 };
+
+struct GemmMaps {
+  CUtensorMap a;      // weights; fp8 box [128 B x 128 (64 for SiLU) rows], e2m1x2 box [64 B x rows]
+  CUtensorMap b[4];   // tokens; box rows 16 / 32 / 64 / 128
+};
+
+struct GemmParams {
+  int M;              // dense: tokens; grouped: compact rows S
+  int N;              // dense: weight rows; grouped: rows of one expert matrix (2N or K)
+  int K;
+  int nkb;            // ceil(K / 128)
+  int tiles_n;
+  int tiles_m;
+  int splits;
+  int kb_per_split;
+  // grouped (MoE) work description, produced on the device by moe_align
+  int grouped;
+  const int* num_blocks;
+  const int* expert_ids;
+  const int* offsets;
+  const int* sorted_ids;
+  int block_m;
+  int narrow_max;     // blocks with m_size <= narrow_max use the narrowest legal MMA N
+  int n_half;         // SiLU stage: intermediate size N (gate rows = [0, N))
+  // scales
+  const float* a_scale;
+  int64_t sa0, sa1;
+  const float* w_scale;
+  int64_t sw0, sw1, sw_e;
+  int block_n;        // 0 = per-tensor (w_scale[0]); 1 or 128 = block rows
+  const uint8_t* mx_scale;
+  int64_t mx_ld;
+  int mx_cols;
+  int64_t mx_rows_total;
+  const void* bias;
+  int bias_dtype;
+  int64_t bias_e;
+  const float* route_w;
+  void* out;
+  int out_dtype;
+  int64_t ldo;
+  float* partial;
+  int* status;
+  unsigned long long budget_ns;
+  int inject_stall;
+  int vec_ok;
+};
+
+template <int KIND, int BT>
+struct Layout {
+  static constexpr int kThreads = (KIND == KIND_F8F8) ? 256 : 384;
+  static constexpr int A_BYTES = (KIND == KIND_MXW) ? 128 * 64 : 128 * 128;
+  static constexpr int B_BYTES = BT * 128 * ((KIND == KIND_F8F8) ? 1 : 2);
+  static constexpr int C_BYTES = (KIND == KIND_F8F8) ? 0 : 128 * 256;
+  static constexpr int CS = (KIND == KIND_F8F8) ? 0 : 2;
+  static constexpr int OUT_BYTES = 32 * 128 * 4;
+  static constexpr int MISC_BYTES = 2048;
+  static constexpr int BUDGET = 225 * 1024 - 1024;   // minus alignment slack
+  static constexpr int FIXED = OUT_BYTES + MISC_BYTES + CS * C_BYTES;
+  // F8F8: A and B stages in lock step; bf16 kinds: B ring 4 deep when it fits
+  static constexpr int BS_PREF =
+      (KIND == KIND_F8F8) ? 0 : (B_BYTES * 4 + 4 * A_BYTES + FIXED <= BUDGET ? 4 : 2);
+  static constexpr int AS_RAW =
+      (KIND == KIND_F8F8) ? (BUDGET - FIXED) / (A_BYTES + B_BYTES)
+                          : (BUDGET - FIXED - BS_PREF * B_BYTES) / A_BYTES;
+  static constexpr int AS = AS_RAW > 12 ? 12 : AS_RAW;
+  static constexpr int BS = (KIND == KIND_F8F8) ? AS : BS_PREF;
+  static constexpr int TOTAL = AS * A_BYTES + CS * C_BYTES + BS * B_BYTES + OUT_BYTES + MISC_BYTES;
+  static constexpr int TMEM_COLS = 2 * BT;
+  static_assert(AS >= 2 && BS >= 2, "pipeline too shallow");
+  static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory over budget");
+};
+
+struct Unit {
+  int n0;       // first weight row of the tile inside its matrix (scales, bias, output)
+  int m0;       // first token row (dense) / compact row (grouped)
+  int rows;     // valid token columns
+  int kb0, kb1;
+  int e;        // expert (grouped) or 0
+  int blk;      // expert block (grouped)
+  int split;
+  int tn;
+  int wrow0, wrow1;   // TMA row coordinates of the weight box(es)
+  int n_inst;   // MMA instruction N
+  int bvar;     // token box variant (rows 16 << bvar)
+};
+
+__device__ __forceinline__ int box_variant(int n) {
+  return n <= 16 ? 0 : (n <= 32 ? 1 : (n <= 64 ? 2 : 3));
+}
+
+template <int EPI, int BT>
+__device__ __forceinline__ Unit get_unit(const GemmParams& p, int u) {
+  Unit U;
+  if (!p.grouped) {
+    const int per = p.tiles_m * p.splits;
+    U.tn = u / per;
+    const int r = u - U.tn * per;
+    const int tm = r / p.splits;
+    U.split = r - tm * p.splits;
+    U.n0 = U.tn * 128;
+    U.m0 = tm * BT;
+    U.rows = min(BT, p.M - U.m0);
+    U.kb0 = U.split * p.kb_per_split;
+    U.kb1 = min(p.nkb, U.kb0 + p.kb_per_split);
+    U.e = 0;
+    U.blk = 0;
+    U.wrow0 = U.n0;
+    U.wrow1 = U.n0;
+    U.n_inst = BT;
+    U.bvar = box_variant(BT);
+  } else {
+    U.blk = u / p.tiles_n;
+    U.tn = u - U.blk * p.tiles_n;
+    U.split = 0;
+    U.e = __ldg(p.expert_ids + U.blk);
+    U.m0 = __ldg(p.offsets + U.blk);
+    U.rows = __ldg(p.offsets + U.blk + 1) - U.m0;
+    U.kb0 = 0;
+    U.kb1 = p.nkb;
+    const int64_t base = static_cast<int64_t>(U.e) * p.N;
+    if (EPI == EPI_SILU) {
+      U.n0 = U.tn * 64;
+      U.wrow0 = static_cast<int>(base + U.n0);
+      U.wrow1 = static_cast<int>(base + p.n_half + U.n0);
+    } else {
+      U.n0 = U.tn * 128;
+      U.wrow0 = static_cast<int>(base + U.n0);
+      U.wrow1 = U.wrow0;
+    }
+    // per-block instruction shape: the narrowest legal N (multiple of 16)
+    // that covers the block, or the full tile width
+    const int fit = ((U.rows + 15) / 16) * 16;
+    U.n_inst = (U.rows <= p.narrow_max) ? min(fit, BT) : BT;
+    U.bvar = box_variant(U.n_inst);
+  }
+  return U;
+}
+
+// weight row (inside its matrix) held by TMEM lane `lane` of the tile
+template <int EPI>
+__device__ __forceinline__ int lane_row(const GemmParams& p, const Unit& U, int lane) {
+  if (EPI == EPI_SILU) return lane < 64 ? U.n0 + lane : p.n_half + U.n0 + (lane - 64);
+  return U.n0 + lane;
+}
+
+template <int EPI>
+__device__ __forceinline__ bool lane_row_valid(const GemmParams& p, const Unit& U, int lane) {
+  if (EPI == EPI_SILU) return U.n0 + (lane & 63) < p.n_half;
+  return U.n0 + lane < p.N;
+}
+
+__device__ __forceinline__ float load_bias(const GemmParams& p, int64_t idx) {
+  if (p.bias == nullptr) return 0.f;
+  if (p.bias_dtype == DT_BF16)
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.bias)[idx]);
+  return reinterpret_cast<const float*>(p.bias)[idx];
+}
+
+// ------------------------------------------------------------ weight decode
+// e4m3 pair -> bf16 pair, exactly: the pair is first widened to f16 (every
+// e4m3 value is a normal f16 or zero), whose bits shifted right by 3 form a
+// bf16 with the same mantissa and a biased exponent 112 short; one bf16
+// multiply by 2^112 restores it (zero stays zero).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
+  uint32_t t = ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&t);
+  const uint32_t k2 = 0x77807780u;   // bf16 pair (2^112, 2^112)
+  v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&k2));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// e2m1 pair (one byte, low nibble first) -> bf16 pair times the block scale
+// pair `sc` (already including 2^112, see above).
+__device__ __forceinline__ uint32_t e2m1x2_to_bf16x2(uint32_t byte, __nv_bfloat162 sc) {
+  uint32_t h;
+  asm("{ .reg .b8 t; .reg .b16 s; cvt.u16.u32 s, %1; cvt.u8.u16 t, s;"
+      " cvt.rn.f16x2.e2m1x2 %0, t; }"
+      : "=r"(h)
+      : "r"(byte));
+  uint32_t t = ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&t);
+  v = __hmul2(v, sc);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------------ kernel
+template <int KIND, int EPI, int BT, bool PROMOTE>
+__global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  using L = Layout<KIND, BT>;
+  constexpr int AS = L::AS, BS = L::BS, CS = L::CS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sC = sA + AS * L::A_BYTES;
+  uint8_t* sB = sC + CS * L::C_BYTES;
+  float* sOut = reinterpret_cast<float*>(sB + BS * L::B_BYTES);
+  uint8_t* misc = reinterpret_cast<uint8_t*>(sOut) + L::OUT_BYTES;
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(misc);
+  uint64_t* a_empty = a_full + 12;
+  uint64_t* b_full = a_empty + 12;
+  uint64_t* b_empty = b_full + 12;
+  uint64_t* c_full = b_empty + 12;
+  uint64_t* c_empty = c_full + 2;
+  uint64_t* t_full = c_empty + 2;
+  uint64_t* t_empty = t_full + 2;
+  uint64_t* drain = t_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  float* sAs = reinterpret_cast<float*>(misc + 1024);    // [2][BT] column scales
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  WaitCtx wc{p.status, abort_flag, p.budget_ns};
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < AS; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], KIND == KIND_F8F8 ? 1 : 4);
+    }
+    for (int i = 0; i < BS; ++i) {
+      mbar_init(&b_full[i], 1);
+      mbar_init(&b_empty[i], 1);
+    }
+    for (int i = 0; i < CS; ++i) {
+      mbar_init(&c_full[i], 4);
+      mbar_init(&c_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&t_full[i], 1);
+      mbar_init(&t_empty[i], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.a);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total =
+      p.grouped ? __ldg(p.num_blocks) * p.tiles_n : p.tiles_n * p.tiles_m * p.splits;
+
+  if (warp == 0) {
+    // ------------------------------------------------ weight producer
+    if (lane == 0 && !p.inject_stall) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t it = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit U = get_unit<EPI, BT>(p, u);
+        for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
+          const int s = it % AS;
+          if (!mbar_wait(&a_empty[s], ((it / AS) & 1) ^ 1, wc)) goto prod_a_done;
+          mbar_expect_tx(&a_full[s], L::A_BYTES);
+          const int kc = (KIND == KIND_MXW) ? kb * 64 : kb * 128;
+          uint8_t* dst = sA + s * L::A_BYTES;
+          if (EPI == EPI_SILU) {
+            tma_load_2d_hint(dst, &maps.a, &a_full[s], kc, U.wrow0, pol);
+            tma_load_2d_hint(dst + L::A_BYTES / 2, &maps.a, &a_full[s], kc, U.wrow1, pol);
+          } else {
+            tma_load_2d_hint(dst, &maps.a, &a_full[s], kc, U.wrow0, pol);
+          }
+        }
+      }
+    prod_a_done:
+      if (*abort_flag) {
+        // let every copy already issued land before the CTA goes away
+        volatile int zero = 0;
+        WaitCtx dw{p.status, &zero, 1000000000ull};
+        const uint32_t first = it > static_cast<uint32_t>(AS) ? it - AS : 0;
+        for (uint32_t i = first; i < it; ++i) mbar_wait(&a_full[i % AS], (i / AS) & 1, dw);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------- token producer
+    if (lane == 0 && !p.inject_stall) {
+      uint32_t it = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit U = get_unit<EPI, BT>(p, u);
+        const int brows = 16 << U.bvar;
+        const CUtensorMap* mb = &maps.b[U.bvar];
+        for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
+          const int s = it % BS;
+          if (!mbar_wait(&b_empty[s], ((it / BS) & 1) ^ 1, wc)) goto prod_b_done;
+          uint8_t* dst = sB + s * L::B_BYTES;
+          if (KIND == KIND_F8F8) {
+            mbar_expect_tx(&b_full[s], brows * 128);
+            tma_load_2d(dst, mb, &b_full[s], kb * 128, U.m0);
+          } else {
+            mbar_expect_tx(&b_full[s], brows * 256);
+            tma_load_2d(dst, mb, &b_full[s], kb * 128, U.m0);
+            tma_load_2d(dst + brows * 128, mb, &b_full[s], kb * 128 + 64, U.m0);
+          }
+        }
+      }
+    prod_b_done:
+      if (*abort_flag) {
+        volatile int zero = 0;
+        WaitCtx dw{p.status, &zero, 1000000000ull};
+        const uint32_t first = it > static_cast<uint32_t>(BS) ? it - BS : 0;
+        for (uint32_t i = first; i < it; ++i) mbar_wait(&b_full[i % BS], (i / BS) & 1, dw);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t ia = 0, ib = 0, au = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit U = get_unit<EPI, BT>(p, u);
+        const int brows = 16 << U.bvar;
+        const uint32_t idesc =
+            (KIND == KIND_F8F8) ? idesc_e4m3(128, U.n_inst) : idesc_bf16(128, U.n_inst);
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
+          const bool first = (kb == U.kb0), last = (kb == U.kb1 - 1);
+          const uint32_t buf = au & 1;
+          if (PROMOTE || first)
+            if (!mbar_wait(&t_empty[buf], ((au >> 1) & 1) ^ 1, wc)) goto mma_done;
+          const int sa = (KIND == KIND_F8F8) ? ia % AS : ia % CS;
+          if (KIND == KIND_F8F8) {
+            if (!mbar_wait(&a_full[sa], (ia / AS) & 1, wc)) goto mma_done;
+          } else {
+            if (!mbar_wait(&c_full[sa], (ia / CS) & 1, wc)) goto mma_done;
+          }
+          const int sb = ib % BS;
+          if (!mbar_wait(&b_full[sb], (ib / BS) & 1, wc)) goto mma_done;
+          tc_fence_after();
+          const uint32_t d = tmem_base + buf * BT;
+          if (KIND == KIND_F8F8) {
+            const uint32_t a0 = smem_u32(sA + sa * L::A_BYTES);
+            const uint32_t b0 = smem_u32(sB + sb * L::B_BYTES);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t acc = PROMOTE ? (j > 0) : (!first || j > 0);
+              mma_f8f6f4(d, sw128_desc(a0 + 32 * j), sw128_desc(b0 + 32 * j), idesc, acc);
+            }
+            mma_commit(&a_empty[sa]);
+          } else {
+            const uint32_t a0 = smem_u32(sC + sa * L::C_BYTES);
+            const uint32_t b0 = smem_u32(sB + sb * L::B_BYTES);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t acc = PROMOTE ? (j > 0) : (!first || j > 0);
+              const uint32_t ao = a0 + (j >> 2) * 16384 + (j & 3) * 32;
+              const uint32_t bo = b0 + (j >> 2) * (brows * 128) + (j & 3) * 32;
+              mma_f16(d, sw128_desc(ao), sw128_desc(bo), idesc, acc);
+            }
+            mma_commit(&c_empty[sa]);
+          }
+          mma_commit(&b_empty[sb]);
+          ++ia;
+          ++ib;
+          if (PROMOTE || last) {
+            mma_commit(&t_full[buf]);
+            ++au;
+          }
+        }
+      }
+    mma_done:
+      if (*abort_flag) {
+        mma_commit(drain);
+        volatile int zero = 0;
+        WaitCtx dw{p.status, &zero, 1000000000ull};
+        mbar_wait(drain, 0, dw);
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------- weight decode to bf16
+    if (KIND != KIND_F8F8) {
+      const int ct = threadIdx.x - 256;
+      uint32_t ia = 0, ic = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit U = get_unit<EPI, BT>(p, u);
+        for (int kb = U.kb0; kb < U.kb1; ++kb, ++ia, ++ic) {
+          const int sa = ia % AS, sc = ic % CS;
+          if (!mbar_wait(&a_full[sa], (ia / AS) & 1, wc)) goto conv_done;
+          if (!mbar_wait(&c_empty[sc], ((ic / CS) & 1) ^ 1, wc)) goto conv_done;
+          const uint8_t* src = sA + sa * L::A_BYTES;
+          uint8_t* dst = sC + sc * L::C_BYTES;
+          if (KIND == KIND_F8W) {
+            // 1024 chunks of 16 fp8 (row r, chunk c); swizzled source rows
+#pragma unroll 2
+            for (int i = 0; i < 8; ++i) {
+              const int q = i * 128 + ct;
+              const int r = q >> 3, c = q & 7;
+              const uint4 raw =
+                  *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
+              uint4 o0, o1;
+              o0.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.x));
+              o0.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.x >> 16));
+              o0.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.y));
+              o0.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.y >> 16));
+              o1.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.z));
+              o1.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.z >> 16));
+              o1.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.w));
+              o1.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.w >> 16));
+              const int h = c >> 2, cc = (c & 3) * 2;
+              uint8_t* rowp = dst + h * 16384 + r * 128;
+              *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = o0;
+              *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ (r & 7)) << 4)) = o1;
+            }
+          } else {
+            // 512 chunks of 32 e2m1 (row r, 32-element group c), linear source
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+              const int q = i * 128 + ct;
+              const int r = q >> 2, c = q & 3;
+              const uint4 raw = *reinterpret_cast<const uint4*>(src + q * 16);
+              // ue8m0 scale of this 32-element group
+              int64_t grow;
+              if (EPI == EPI_SILU)
+                grow = static_cast<int64_t>(r < 64 ? U.wrow0 + r : U.wrow1 + (r - 64));
+              else
+                grow = static_cast<int64_t>(U.wrow0) + r;
+              if (grow >= p.mx_rows_total) grow = p.mx_rows_total - 1;
+              const int col = kb * 4 + c;
+              uint32_t e = 127;
+              if (col < p.mx_cols) e = __ldg(p.mx_scale + grow * p.mx_ld + col);
+              // bf16 2^(e - 127 + 112) when representable; else two steps
+              __nv_bfloat162 sc;
+              uint32_t two_step = 0;
+              {
+                const int ex = static_cast<int>(e) + 112;  // biased bf16 exponent of 2^(e-15)
+                if (ex >= 1 && ex <= 254) {
+                  const uint32_t bits = (static_cast<uint32_t>(ex) << 7) * 0x10001u;
+                  sc = *reinterpret_cast<const __nv_bfloat162*>(&bits);
+                } else {
+                  two_step = 1;
+                  const uint32_t bits = 0x77807780u;
+                  sc = *reinterpret_cast<const __nv_bfloat162*>(&bits);
+                }
+              }
+              uint32_t w[16];
+              const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb)
+                  w[j * 4 + bb] = e2m1x2_to_bf16x2((in[j] >> (8 * bb)) & 0xFFu, sc);
+              }
+              if (two_step) {
+                const float f = ldexpf(1.0f, static_cast<int>(e) - 127);
+                const __nv_bfloat162 s2 = __floats2bfloat162_rn(f, f);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w[j]);
+                  v = __hmul2(v, s2);
+                  w[j] = *reinterpret_cast<uint32_t*>(&v);
+                }
+              }
+              const int h = c >> 1, cc0 = (c & 1) * 4;
+              uint8_t* rowp = dst + h * 16384 + r * 128;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint4 o;
+                o.x = w[j * 4 + 0];
+                o.y = w[j * 4 + 1];
+                o.z = w[j * 4 + 2];
+                o.w = w[j * 4 + 3];
+                *reinterpret_cast<uint4*>(rowp + (((cc0 + j) ^ (r & 7)) << 4)) = o;
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&c_full[sc]);
+            mbar_arrive(&a_empty[sa]);
+          }
+        }
+      }
+    conv_done:;
+    }
+  } else if (warp >= 4) {
+    // --------------------------------------------------------- epilogue
+    const int et = threadIdx.x - 128;                 // TMEM lane 0..127
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t au = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const Unit U = get_unit<EPI, BT>(p, u);
+      const int nch = (U.rows + 31) >> 5;
+      const int wr = lane_row<EPI>(p, U, et);
+      const bool wr_ok = lane_row_valid<EPI>(p, U, et);
+      float acc[BT];
+      float fscale = 1.f;
+      if (PROMOTE) {
+#pragma unroll
+        for (int j = 0; j < BT; ++j) acc[j] = 0.f;
+        const int64_t wrc = wr_ok ? wr : 0;
+        auto ws_at = [&](int kb) -> float {
+          if (p.block_n == 0) return __ldg(p.w_scale);
+          return __ldg(p.w_scale + U.e * p.sw_e + (wrc / p.block_n) * p.sw0 + kb * p.sw1);
+        };
+        auto as_at = [&](int kb) -> float {
+          if (p.a_scale == nullptr || et >= U.rows) return 1.f;
+          return __ldg(p.a_scale + static_cast<int64_t>(U.m0 + et) * p.sa0 + kb * p.sa1);
+        };
+        float as_nx = as_at(U.kb0);
+        float ws_nx = ws_at(U.kb0);
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
+          float* sa = sAs + (kb & 1) * BT;
+          if (et < BT) sa[et] = as_nx;
+          const float ws = ws_nx;
+          named_bar_sync(1, 128);
+          if (kb + 1 < U.kb1) {
+            as_nx = as_at(kb + 1);
+            ws_nx = ws_at(kb + 1);
+          }
+          const uint32_t buf = au & 1;
+          if (!mbar_wait(&t_full[buf], (au >> 1) & 1, wc)) goto epi_done;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < BT / 32; ++c) {
+            if (c < nch) {
+              float v[32];
+              tmem_ld32(tmem_base + lane_addr + buf * BT + c * 32, v);
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                acc[c * 32 + j] = fmaf(v[j], ws * sa[c * 32 + j], acc[c * 32 + j]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&t_empty[buf]);
+          ++au;
+        }
+      } else {
+        if (p.block_n == 0 && p.w_scale != nullptr) fscale = __ldg(p.w_scale);
+        const uint32_t buf = au & 1;
+        if (!mbar_wait(&t_full[buf], (au >> 1) & 1, wc)) goto epi_done;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < BT / 32; ++c) {
+          if (c < nch) tmem_ld32(tmem_base + lane_addr + buf * BT + c * 32, &acc[c * 32]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&t_empty[buf]);
+        ++au;
+      }
+      // ------------------------------------------------------- output
+      {
+        float bias_g = 0.f, bias_u = 0.f;
+        if (EPI == EPI_SILU) {
+          const int l = et & 63;
+          if (U.n0 + l < p.n_half && p.bias != nullptr) {
+            bias_g = load_bias(p, U.e * p.bias_e + U.n0 + l);
+            bias_u = load_bias(p, U.e * p.bias_e + p.n_half + U.n0 + l);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < BT / 32; ++c) {
+          if (c < nch) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sOut[j * 128 + et] = acc[c * 32 + j] * fscale;
+            named_bar_sync(1, 128);
+            if (EPI == EPI_DENSE) {
+              const int nl = (et & 31) * 4;
+              const int n = U.n0 + nl;
+              for (int jj = et >> 5; jj < 32; jj += 4) {
+                const int col = c * 32 + jj;
+                if (col >= U.rows) break;
+                const int m = U.m0 + col;
+                const float4 v = *reinterpret_cast<const float4*>(&sOut[jj * 128 + nl]);
+                float vv[4] = {v.x, v.y, v.z, v.w};
+                if (p.splits > 1) {
+                  float* dstp = p.partial + (static_cast<int64_t>(U.split) * p.M + m) * p.N;
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    if (n + i < p.N) dstp[n + i] = vv[i];
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    if (n + i < p.N) vv[i] += load_bias(p, n + i);
+                  const int64_t o = static_cast<int64_t>(m) * p.ldo + n;
+                  if (p.out_dtype == DT_BF16) {
+                    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
+                    if (p.vec_ok && n + 3 < p.N) {
+                      __nv_bfloat162 lo = __floats2bfloat162_rn(vv[0], vv[1]);
+                      __nv_bfloat162 hi = __floats2bfloat162_rn(vv[2], vv[3]);
+                      uint2 pk;
+                      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+                      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+                      *reinterpret_cast<uint2*>(dst) = pk;
+                    } else {
+#pragma unroll
+                      for (int i = 0; i < 4; ++i)
+                        if (n + i < p.N) dst[i] = __float2bfloat16_rn(vv[i]);
+                    }
+                  } else {
+                    float* dst = reinterpret_cast<float*>(p.out) + o;
+                    if (p.vec_ok && n + 3 < p.N) {
+                      *reinterpret_cast<float4*>(dst) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+                    } else {
+#pragma unroll
+                      for (int i = 0; i < 4; ++i)
+                        if (n + i < p.N) dst[i] = vv[i];
+                    }
+                  }
+                }
+              }
+            } else if (EPI == EPI_SILU) {
+              const int l = et & 63;
+              const bool ok = U.n0 + l < p.n_half;
+              for (int jj = et >> 6; jj < 32; jj += 2) {
+                const int col = c * 32 + jj;
+                if (col >= U.rows) break;
+                if (ok) {
+                  const float g = sOut[jj * 128 + l] + bias_g;
+                  const float up = sOut[jj * 128 + 64 + l] + bias_u;
+                  const float a = g / (1.0f + expf(-g)) * up;
+                  reinterpret_cast<__nv_bfloat16*>(p.out)[static_cast<int64_t>(U.m0 + col) * p.ldo +
+                                                          U.n0 + l] = __float2bfloat16_rn(a);
+                }
+              }
+            } else {  // EPI_SCATTER
+              const int nl = (et & 31) * 4;
+              const int n = U.n0 + nl;
+              for (int jj = et >> 5; jj < 32; jj += 4) {
+                const int col = c * 32 + jj;
+                if (col >= U.rows) break;
+                const int slot =
+                    __ldg(p.sorted_ids + static_cast<int64_t>(U.blk) * p.block_m + col);
+                const float rw = __ldg(p.route_w + slot);
+                const float4 v = *reinterpret_cast<const float4*>(&sOut[jj * 128 + nl]);
+                const float vv[4] = {v.x, v.y, v.z, v.w};
+                float* dst = reinterpret_cast<float*>(p.out) + static_cast<int64_t>(slot) * p.ldo;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  if (n + i < p.N) dst[n + i] = (vv[i] + load_bias(p, U.e * p.bias_e + n + i)) * rw;
+              }
+            }
+            named_bar_sync(1, 128);
+          }
+        }
+      }
+    }
+  epi_done:;
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+}  // namespace mxq

@@ -1,0 +1,38 @@
+// gemm_launch.cuh — host-side launch of one gemm_kernel instantiation.
+#pragma once
+
+#include "internal.h"
+
+namespace mxq {
+
+template <int KIND, int EPI, int BT, bool PROMOTE>
+cudaError_t launch_gemm_inst(const GemmMaps& maps, const GemmParams& p, int grid,
+                             cudaStream_t stream) {
+  using L = Layout<KIND, BT>;
+  const int smem = L::TOTAL + 1024;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(gemm_kernel<KIND, EPI, BT, PROMOTE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  gemm_kernel<KIND, EPI, BT, PROMOTE><<<grid, L::kThreads, smem, stream>>>(maps, p);
+  return cudaGetLastError();
+}
+
+template <int KIND, int EPI, bool PROMOTE>
+cudaError_t launch_gemm_bt(int bt, const GemmMaps& maps, const GemmParams& p, int grid,
+                           cudaStream_t stream) {
+  switch (bt) {
+    case 32: return launch_gemm_inst<KIND, EPI, 32, PROMOTE>(maps, p, grid, stream);
+    case 64: return launch_gemm_inst<KIND, EPI, 64, PROMOTE>(maps, p, grid, stream);
+    case 128: return launch_gemm_inst<KIND, EPI, 128, PROMOTE>(maps, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mxq

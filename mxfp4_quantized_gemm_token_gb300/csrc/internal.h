@@ -1,0 +1,58 @@
+// internal.h — host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "gemm_kernel.cuh"
+
+namespace mxq {
+
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  int* status = nullptr;   // device status word (static __device__ variable)
+};
+
+// Per-device facts, checked once per device (compute capability 10.3).
+bool device_info(DeviceInfo* info, std::string* err);
+
+// Process-wide options (see MXQ_OPT_*).
+int64_t option(int32_t which);
+
+// tensor-map encode through the driver entry point (no libcuda link)
+bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                 uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle swizzle, std::string* err);
+
+cudaError_t launch_gemm(int kind, int epi, int bt, bool promote, const GemmMaps& maps,
+                        const GemmParams& p, int grid, cudaStream_t stream);
+
+cudaError_t launch_group_quant(const void* x, int64_t M, int64_t K, int64_t ldx, int group,
+                               float eps, void* q, float* scales, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_moe_align(const int32_t* topk_ids, int64_t S, int32_t E, int32_t block_m,
+                             int32_t* sorted_ids, int32_t* expert_ids, int32_t* offsets,
+                             int32_t* num_blocks, int64_t cap, int* status, cudaStream_t stream);
+
+cudaError_t launch_gather_rows(const void* hidden, int64_t ldh, int64_t K, int32_t topk,
+                               const int32_t* sorted_ids, const int32_t* offsets,
+                               const int32_t* num_blocks, int32_t block_m, int64_t cap, void* xs,
+                               cudaStream_t stream);
+
+cudaError_t launch_combine(const float* y, int64_t T, int32_t topk, int64_t K, void* out,
+                           int64_t ldo, cudaStream_t stream);
+
+cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t M, int64_t N,
+                                 const void* bias, int bias_dtype, void* out, int out_dtype,
+                                 int64_t ldo, cudaStream_t stream);
+
+cudaError_t launch_unsort_rows(const void* ic1, int64_t N, const int32_t* sorted_ids,
+                               const int32_t* offsets, const int32_t* num_blocks, int32_t block_m,
+                               int64_t cap, void* act_out, cudaStream_t stream);
+
+}  // namespace mxq

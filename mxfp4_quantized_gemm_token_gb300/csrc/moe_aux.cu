@@ -1,0 +1,284 @@
+// moe_aux.cu — the non-GEMM steps of the routed MoE path: expert-block
+// alignment, the token-row gather that feeds stage 1, the top-k combine, and
+// the small helpers (split-K reduction of fp8_scaled_mm, debug unsort).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace mxq {
+
+// ------------------------------------------------------------ moe_align
+// "[CPU] routed FP8/MXFP4 MoE" consumes, per expert block mb: expert_ids[mb],
+// the block's token slots sorted_ids[mb*block_m + m] and the compact row
+// offsets[mb]; this kernel produces them.  One CTA of 1024 threads:
+//   1. histogram of slots per expert (shared-memory atomics);
+//   2. exclusive scans: first block and first compact row of each expert;
+//   3. the block table (expert_ids, offsets);
+//   4. a stable ranking of the slots, 1024 at a time in slot order: inside a
+//      warp, lanes with the same expert find each other with match.any and
+//      rank by lane; across warps, per-warp counts in shared memory give the
+//      offset; a running count per expert carries over between chunks.
+// The result is unique (stable order), so it is compared bit for bit.
+__global__ void __launch_bounds__(1024) moe_align_kernel(const int32_t* __restrict__ ids, int S,
+                                                         int E, int BM, int cap,
+                                                         int32_t* __restrict__ sorted_ids,
+                                                         int32_t* __restrict__ expert_ids,
+                                                         int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ num_blocks,
+                                                         int* status) {
+  extern __shared__ int sm[];
+  int* cnt = sm;
+  int* blk_start = cnt + E;
+  int* pos_start = blk_start + E;
+  int* run = pos_start + E;
+  int* wcnt = run + E;   // [32][E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  for (int i = tid; i < E; i += 1024) {
+    cnt[i] = 0;
+    run[i] = 0;
+  }
+  for (int i = tid; i < 32 * E; i += 1024) wcnt[i] = 0;
+  for (int64_t i = tid; i < static_cast<int64_t>(cap) * BM; i += 1024) sorted_ids[i] = S;
+  for (int i = tid; i < cap; i += 1024) expert_ids[i] = -1;
+  for (int i = tid; i <= cap; i += 1024) offsets[i] = S;
+  __syncthreads();
+
+  bool bad = false;
+  for (int s = tid; s < S; s += 1024) {
+    const int e = __ldg(ids + s);
+    if (e >= 0 && e < E)
+      atomicAdd(&cnt[e], 1);
+    else
+      bad = true;
+  }
+  if (bad) atomicOr(status, kStatusBadIndex);
+  __syncthreads();
+
+  if (tid == 0) {
+    int b = 0, pos = 0;
+    for (int e = 0; e < E; ++e) {
+      blk_start[e] = b;
+      pos_start[e] = pos;
+      b += (cnt[e] + BM - 1) / BM;
+      pos += cnt[e];
+    }
+    *num_blocks = b;
+    offsets[b] = pos;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += 1024) {
+    const int nb = (cnt[e] + BM - 1) / BM;
+    for (int j = 0; j < nb; ++j) {
+      expert_ids[blk_start[e] + j] = e;
+      offsets[blk_start[e] + j] = pos_start[e] + j * BM;
+    }
+  }
+
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = 0; base < S; base += 1024) {
+    const int s = base + tid;
+    int e = (s < S) ? __ldg(ids + s) : -1;
+    const bool valid = e >= 0 && e < E;
+    if (!valid) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    const bool leader = (__ffs(peers) - 1) == lane;
+    if (valid && leader) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      int pos = run[e] + rank;
+      for (int w = 0; w < warp; ++w) pos += wcnt[w * E + e];
+      sorted_ids[static_cast<int64_t>(blk_start[e]) * BM + pos] = s;
+    }
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += 1024) {
+      int t = 0;
+      for (int w = 0; w < 32; ++w) t += wcnt[w * E + ee];
+      run[ee] += t;
+    }
+    __syncthreads();
+    if (valid && leader) wcnt[warp * E + e] = 0;
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_moe_align(const int32_t* topk_ids, int64_t S, int32_t E, int32_t block_m,
+                             int32_t* sorted_ids, int32_t* expert_ids, int32_t* offsets,
+                             int32_t* num_blocks, int64_t cap, int* status, cudaStream_t stream) {
+  const int smem = static_cast<int>((4 + 32) * E * sizeof(int));
+  if (smem > 48 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(moe_align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  moe_align_kernel<<<1, 1024, smem, stream>>>(topk_ids, static_cast<int>(S), E, block_m,
+                                              static_cast<int>(cap), sorted_ids, expert_ids,
+                                              offsets, num_blocks, status);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ row gather
+// Stage-1 operand: compact row r = offsets[b] + m holds hidden[slot / topk],
+// slot = sorted_ids[b*block_m + m] (the page copies the same rows per block
+// before its first N tile).  One warp per (block, row) position.
+__global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int64_t ldh, int64_t K,
+                                   int topk, const int32_t* __restrict__ sorted_ids,
+                                   const int32_t* __restrict__ offsets,
+                                   const int32_t* __restrict__ num_blocks, int BM,
+                                   __nv_bfloat16* __restrict__ xs, int vec) {
+  const int nb = __ldg(num_blocks);
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t total = static_cast<int64_t>(nb) * BM;
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total;
+       w += nwarps) {
+    const int b = static_cast<int>(w / BM), m = static_cast<int>(w % BM);
+    const int r0 = __ldg(offsets + b);
+    if (m >= __ldg(offsets + b + 1) - r0) continue;
+    const int slot = __ldg(sorted_ids + w);
+    const __nv_bfloat16* src = hidden + static_cast<int64_t>(slot / topk) * ldh;
+    __nv_bfloat16* dst = xs + static_cast<int64_t>(r0 + m) * K;
+    if (vec) {
+      for (int64_t k = lane * 8; k < K; k += 256)
+        *reinterpret_cast<uint4*>(dst + k) = __ldg(reinterpret_cast<const uint4*>(src + k));
+    } else {
+      for (int64_t k = lane; k < K; k += 32) dst[k] = src[k];
+    }
+  }
+}
+
+cudaError_t launch_gather_rows(const void* hidden, int64_t ldh, int64_t K, int32_t topk,
+                               const int32_t* sorted_ids, const int32_t* offsets,
+                               const int32_t* num_blocks, int32_t block_m, int64_t cap, void* xs,
+                               cudaStream_t stream) {
+  const int vec = (K % 8 == 0) && (ldh % 8 == 0) &&
+                  (reinterpret_cast<uintptr_t>(hidden) & 15) == 0 &&
+                  (reinterpret_cast<uintptr_t>(xs) & 15) == 0;
+  const int64_t warps = cap * block_m;
+  int64_t blocks = (warps + 7) / 8;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  gather_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const __nv_bfloat16*>(hidden), ldh, K, topk, sorted_ids, offsets,
+      num_blocks, block_m, reinterpret_cast<__nv_bfloat16*>(xs), vec);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ combine
+// out[t] = bf16( sum_{k=0..topk-1} y[t*topk + k] ), ascending k, fp32 sum;
+// y already carries the routing weight.
+__global__ void combine_kernel(const float* __restrict__ y, int64_t T, int topk, int64_t K,
+                               __nv_bfloat16* __restrict__ out, int64_t ldo, int vec) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  if (vec) {
+    const int64_t K4 = K / 4;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < T * K4;
+         i += stride) {
+      const int64_t t = i / K4, k = (i - t * K4) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < topk; ++j) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(y + (t * topk + j) * K + k));
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(out + t * ldo + k) = pk;
+    }
+  } else {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < T * K;
+         i += stride) {
+      const int64_t t = i / K, k = i - t * K;
+      float acc = 0.f;
+      for (int j = 0; j < topk; ++j) acc += y[(t * topk + j) * K + k];
+      out[t * ldo + k] = __float2bfloat16_rn(acc);
+    }
+  }
+}
+
+cudaError_t launch_combine(const float* y, int64_t T, int32_t topk, int64_t K, void* out,
+                           int64_t ldo, cudaStream_t stream) {
+  const int vec = (K % 4 == 0) && (ldo % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 7) == 0 &&
+                  (reinterpret_cast<uintptr_t>(y) & 15) == 0;
+  const int64_t n = vec ? T * (K / 4) : T * K;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 8192) blocks = 8192;
+  if (blocks < 1) blocks = 1;
+  combine_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      y, T, topk, K, reinterpret_cast<__nv_bfloat16*>(out), ldo, vec);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------ split-K reduction
+// out[m, n] = round( sum_s partial[s, m, n] + bias[n] ), ascending s.
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int64_t M,
+                                     int64_t N, const void* bias, int bias_dtype, void* out,
+                                     int out_dtype, int64_t ldo) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < M * N;
+       i += stride) {
+    const int64_t m = i / N, n = i - m * N;
+    float acc = 0.f;
+    for (int s = 0; s < splits; ++s) acc += part[s * M * N + i];
+    if (bias != nullptr)
+      acc += (bias_dtype == DT_BF16)
+                 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(bias)[n])
+                 : reinterpret_cast<const float*>(bias)[n];
+    if (out_dtype == DT_BF16)
+      reinterpret_cast<__nv_bfloat16*>(out)[m * ldo + n] = __float2bfloat16_rn(acc);
+    else
+      reinterpret_cast<float*>(out)[m * ldo + n] = acc;
+  }
+}
+
+cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t M, int64_t N,
+                                 const void* bias, int bias_dtype, void* out, int out_dtype,
+                                 int64_t ldo, cudaStream_t stream) {
+  int64_t blocks = (M * N + 255) / 256;
+  if (blocks > 8192) blocks = 8192;
+  if (blocks < 1) blocks = 1;
+  splitk_reduce_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      partial, splits, M, N, bias, bias_dtype, out, out_dtype, ldo);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ debug unsort
+// act_out[slot] = ic1[offsets[b] + m] for slot = sorted_ids[b*block_m + m].
+__global__ void unsort_rows_kernel(const __nv_bfloat16* __restrict__ ic1, int64_t N,
+                                   const int32_t* __restrict__ sorted_ids,
+                                   const int32_t* __restrict__ offsets,
+                                   const int32_t* __restrict__ num_blocks, int BM,
+                                   __nv_bfloat16* __restrict__ act_out) {
+  const int nb = __ldg(num_blocks);
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       w < static_cast<int64_t>(nb) * BM; w += nwarps) {
+    const int b = static_cast<int>(w / BM), m = static_cast<int>(w % BM);
+    const int r0 = __ldg(offsets + b);
+    if (m >= __ldg(offsets + b + 1) - r0) continue;
+    const int slot = __ldg(sorted_ids + w);
+    for (int64_t k = lane; k < N; k += 32)
+      act_out[static_cast<int64_t>(slot) * N + k] = ic1[static_cast<int64_t>(r0 + m) * N + k];
+  }
+}
+
+cudaError_t launch_unsort_rows(const void* ic1, int64_t N, const int32_t* sorted_ids,
+                               const int32_t* offsets, const int32_t* num_blocks, int32_t block_m,
+                               int64_t cap, void* act_out, cudaStream_t stream) {
+  int64_t blocks = (cap * block_m + 7) / 8;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  unsort_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const __nv_bfloat16*>(ic1), N, sorted_ids, offsets, num_blocks, block_m,
+      reinterpret_cast<__nv_bfloat16*>(act_out));
+  return cudaGetLastError();
+}
+
+}  // namespace mxq

@@ -1,0 +1,143 @@
+// quant.cu — per-token-group FP8 quantization of bf16 activations.
+//
+// "[XPU] block-FP8 linear via torch scaled_mm", key code excerpts: when no
+// input scale is given, the activation is quantized per 1 x block_k group
+// (per_token_group_quant_fp8) into e4m3 with one fp32 scale per group,
+// shape [M, K/128].  For each group: s = max(amax, eps) / 448, and every
+// element is q = e4m3(clamp(x / s, -448, 448)), round to nearest even, with
+// IEEE fp32 division (no reciprocal) so the codes are reproducible.
+//
+// Memory-bound: 2 bytes in, 1 + 4/128 bytes out per element.  The fast path
+// gives each 128-element group to a half warp (8 contiguous bf16 = one 16-byte
+// load per lane), reduces amax with shuffles, and writes 8 codes per lane.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace mxq {
+
+__device__ __forceinline__ float clamp448(float t) {
+  // comparisons (not fminf/fmaxf) so a NaN stays NaN
+  t = (t > 448.f) ? 448.f : t;
+  t = (t < -448.f) ? -448.f : t;
+  return t;
+}
+
+// two fp32 -> two e4m3 codes (lo in the low byte), round to nearest even
+__device__ __forceinline__ uint16_t e4m3x2_rn(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// group == 128, K % 128 == 0, 16-byte aligned rows
+__global__ void group_quant128_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K,
+                                      int64_t ldx, float eps, uint8_t* __restrict__ q,
+                                      float* __restrict__ scales) {
+  const int64_t G = K / 128;
+  const int64_t total = M * G;
+  const int lane = threadIdx.x & 31;
+  const int hl = lane & 15;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       2 * w < total; w += nwarps) {
+    const int64_t item = 2 * w + (lane >> 4);
+    const bool valid = item < total;
+    const int64_t m = valid ? item / G : 0;
+    const int64_t g = valid ? item - m * G : 0;
+    float v[8];
+    float amax = 0.f;
+    if (valid) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(x + m * ldx + g * 128 + hl * 8));
+      const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(wv[i] << 16);
+        v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float a = fabsf(v[i]);
+        amax = (a > amax) ? a : amax;
+      }
+    }
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, amax, off);
+      amax = (o > amax) ? o : amax;
+    }
+    if (valid) {
+      const float s = __fdiv_rn((amax > eps) ? amax : eps, 448.f);
+      uint32_t pk[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float* vv = v + 4 * h;
+        const uint16_t a =
+            e4m3x2_rn(clamp448(__fdiv_rn(vv[0], s)), clamp448(__fdiv_rn(vv[1], s)));
+        const uint16_t b =
+            e4m3x2_rn(clamp448(__fdiv_rn(vv[2], s)), clamp448(__fdiv_rn(vv[3], s)));
+        pk[h] = static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
+      }
+      *reinterpret_cast<uint2*>(q + m * K + g * 128 + hl * 8) = make_uint2(pk[0], pk[1]);
+      if (hl == 0) scales[m * G + g] = s;
+    }
+  }
+}
+
+// any group (multiple of 8, <= 1024), ragged K, any row stride: one warp per group
+__global__ void group_quant_generic_kernel(const __nv_bfloat16* __restrict__ x, int64_t M,
+                                           int64_t K, int64_t ldx, int group, float eps,
+                                           uint8_t* __restrict__ q, float* __restrict__ scales) {
+  const int64_t G = (K + group - 1) / group;
+  const int64_t total = M * G;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total;
+       w += nwarps) {
+    const int64_t m = w / G, g = w - (w / G) * G;
+    const int64_t k0 = g * group;
+    const int64_t k1 = (k0 + group < K) ? k0 + group : K;
+    float amax = 0.f;
+    for (int64_t k = k0 + lane; k < k1; k += 32) {
+      const float a = fabsf(__bfloat162float(x[m * ldx + k]));
+      amax = (a > amax) ? a : amax;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, amax, off);
+      amax = (o > amax) ? o : amax;
+    }
+    const float s = __fdiv_rn((amax > eps) ? amax : eps, 448.f);
+    for (int64_t k = k0 + lane; k < k1; k += 32) {
+      const float t = clamp448(__fdiv_rn(__bfloat162float(x[m * ldx + k]), s));
+      q[m * K + k] = static_cast<uint8_t>(e4m3x2_rn(t, 0.f) & 0xFF);
+    }
+    if (lane == 0) scales[m * G + g] = s;
+  }
+}
+
+cudaError_t launch_group_quant(const void* x, int64_t M, int64_t K, int64_t ldx, int group,
+                               float eps, void* q, float* scales, int num_sms,
+                               cudaStream_t stream) {
+  const bool fast = group == 128 && K % 128 == 0 && ldx % 8 == 0 &&
+                    (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+                    (reinterpret_cast<uintptr_t>(q) & 7) == 0;
+  const int threads = 256;
+  const int64_t G = (K + group - 1) / group;
+  const int64_t items = fast ? (M * G + 1) / 2 : M * G;       // warps of work
+  int64_t blocks = (items + (threads / 32) - 1) / (threads / 32);
+  const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (fast)
+    group_quant128_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(x), M, K, ldx, eps,
+        reinterpret_cast<uint8_t*>(q), scales);
+  else
+    group_quant_generic_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(x), M, K, ldx, group, eps,
+        reinterpret_cast<uint8_t*>(q), scales);
+  return cudaGetLastError();
+}
+
+}  // namespace mxq

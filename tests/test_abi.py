@@ -1,0 +1,123 @@
+"""The C-ABI library builds, loads, and exports every symbol include/mxq.h
+declares; host-side argument validation returns its documented status codes
+before touching any device (these calls need no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxq.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxq_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mxfp4_quantized_gemm_token_gb300 import _lib
+    return _lib.load()
+
+
+def test_header_declares_the_four_ops_and_helpers():
+    names = declared_functions()
+    for op in ("mxq_fp8_scaled_mm", "mxq_per_token_group_quant_fp8", "mxq_moe_align_block",
+               "mxq_fused_experts"):
+        assert op in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from mxfp4_quantized_gemm_token_gb300 import _lib
+    names = declared_functions()
+    assert sorted(_lib.EXPORTED) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_options_roundtrip(lib):
+    from mxfp4_quantized_gemm_token_gb300 import _lib
+    assert b"sm_103a" in lib.mxq_version()
+    v = ctypes.c_int64()
+    assert lib.mxq_get_option(_lib.OPT_WAIT_BUDGET_NS, ctypes.byref(v)) == 0
+    old = v.value
+    assert lib.mxq_set_option(_lib.OPT_WAIT_BUDGET_NS, 12345) == 0
+    assert lib.mxq_get_option(_lib.OPT_WAIT_BUDGET_NS, ctypes.byref(v)) == 0 and v.value == 12345
+    assert lib.mxq_set_option(_lib.OPT_WAIT_BUDGET_NS, old) == 0
+    assert lib.mxq_set_option(99, 1) == _lib.ERR_INVALID_ARG
+    assert lib.mxq_set_option(_lib.OPT_FORCE_PATH, 3) == _lib.ERR_INVALID_ARG
+    assert b"FORCE_PATH" in lib.mxq_last_error()
+
+
+FAKE = ctypes.c_void_p(1 << 20)   # never dereferenced: validation fails first
+
+
+def mm(lib, **kw):
+    a = dict(A=FAKE, a_dtype=3, M=4, K=256, lda=256, a_scale=FAKE, sa0=2, sa1=1, W=FAKE, N=128,
+             ldw=256, w_scale=FAKE, block_n=128, block_k=128, sw0=2, sw1=1, bias=None,
+             bias_dtype=0, out=FAKE, out_dtype=1, ldo=128, ws=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return lib.mxq_fp8_scaled_mm(*a.values())
+
+
+def test_scaled_mm_rejects_unsupported_block_sizes(lib):
+    from mxfp4_quantized_gemm_token_gb300 import _lib
+    # MXFP8 [1, 32] and other shapes are refused like the page's block_size check
+    for bn, bk in [(1, 32), (64, 64), (128, 64), (2, 128), (0, 128), (128, 0)]:
+        assert mm(lib, block_n=bn, block_k=bk) == _lib.ERR_UNSUPPORTED
+    assert b"block size" in lib.mxq_last_error()
+
+
+def test_scaled_mm_argument_errors(lib):
+    from mxfp4_quantized_gemm_token_gb300 import _lib
+    assert mm(lib, M=0) == _lib.OK                      # empty problem: nothing to do
+    assert mm(lib, N=0) == _lib.OK
+    assert mm(lib, K=0) == _lib.ERR_INVALID_ARG
+    assert mm(lib, M=-1) == _lib.ERR_INVALID_ARG
+    assert mm(lib, A=None) == _lib.ERR_INVALID_ARG
+    assert mm(lib, a_scale=None) == _lib.ERR_INVALID_ARG   # W8A8 needs group scales
+    assert mm(lib, a_dtype=1) == _lib.ERR_INVALID_ARG      # bf16 A takes no scale
+    assert mm(lib, a_dtype=7) == _lib.ERR_UNSUPPORTED
+    assert mm(lib, out_dtype=3) == _lib.ERR_UNSUPPORTED
+    assert mm(lib, lda=100) == _lib.ERR_INVALID_ARG
+    assert mm(lib, bias=FAKE, bias_dtype=3) == _lib.ERR_UNSUPPORTED
+    assert mm(lib, lda=264) == _lib.ERR_UNSUPPORTED         # row stride not 16-byte multiple
+    assert mm(lib, W=ctypes.c_void_p((1 << 20) + 8)) == _lib.ERR_UNSUPPORTED
+
+
+def test_quant_align_moe_argument_errors(lib):
+    from mxfp4_quantized_gemm_token_gb300 import _lib
+    q = lib.mxq_per_token_group_quant_fp8
+    assert q(FAKE, 0, 128, 128, 128, 1e-10, FAKE, FAKE, None) == _lib.OK
+    assert q(None, 2, 128, 128, 128, 1e-10, FAKE, FAKE, None) == _lib.ERR_INVALID_ARG
+    assert q(FAKE, 2, 128, 64, 128, 1e-10, FAKE, FAKE, None) == _lib.ERR_INVALID_ARG
+    assert q(FAKE, 2, 128, 128, 12, 1e-10, FAKE, FAKE, None) == _lib.ERR_UNSUPPORTED
+    assert q(FAKE, 2, 128, 128, 128, 0.0, FAKE, FAKE, None) == _lib.ERR_INVALID_ARG
+    al = lib.mxq_moe_align_block
+    assert al(FAKE, 4, 2, 8, 48, FAKE, FAKE, FAKE, FAKE, 100, None, 0, None) == _lib.ERR_UNSUPPORTED
+    assert al(FAKE, 4, 2, 2000, 16, FAKE, FAKE, FAKE, FAKE, 100, None, 0, None) == _lib.ERR_UNSUPPORTED
+    assert al(FAKE, 4, 2, 8, 16, FAKE, FAKE, FAKE, FAKE, 1, None, 0, None) == _lib.ERR_INVALID_ARG
+    sz = ctypes.c_size_t()
+    assert lib.mxq_fused_experts_workspace_size(4, 256, 8, 128, 2, 16, 1, ctypes.byref(sz)) == 0
+    assert sz.value > 0
+    fe = lib.mxq_fused_experts
+    args = [FAKE, 4, 256, 256, 1, 8, 128, FAKE, FAKE, None, FAKE, FAKE, None, FAKE, FAKE, 2, 16,
+            FAKE, 256, FAKE, sz.value, None]
+    bad = list(args)
+    bad[16] = 24                                              # block_m
+    assert fe(*bad) == _lib.ERR_UNSUPPORTED
+    bad = list(args)
+    bad[4] = 9                                                # wtype
+    assert fe(*bad) == _lib.ERR_UNSUPPORTED
+    bad = list(args)
+    bad[15] = 9                                               # topk > E
+    assert fe(*bad) == _lib.ERR_INVALID_ARG
+    bad = list(args)
+    bad[20] = 16                                              # workspace too small
+    assert fe(*bad) == _lib.ERR_INVALID_ARG
+    bad = list(args)
+    bad[1] = 0                                                # no tokens
+    assert fe(*bad) == _lib.OK
