@@ -224,6 +224,15 @@ __device__ __forceinline__ uint32_t e2m1x2_to_bf16x2(uint32_t byte, __nv_bfloat1
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Barrier of the 128 epilogue threads on an mbarrier, so that it is bounded
+// like every other wait (a plain bar.sync would hang if one warp gave up).
+__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, const WaitCtx& w) {
+  mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, phase, w);
+  phase ^= 1;
+  return ok;
+}
+
 // ------------------------------------------------------------------ kernel
 template <int KIND, int EPI, int BT, bool PROMOTE>
 __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
@@ -247,7 +256,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
   uint64_t* t_full = c_empty + 2;
   uint64_t* t_empty = t_full + 2;
   uint64_t* drain = t_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* epi_bar = drain + 1;     // bounded barrier of the 128 epilogue threads
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* sAs = reinterpret_cast<float*>(misc + 1024);    // [2][BT] column scales
 
@@ -273,6 +283,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
       mbar_init(&t_empty[i], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(epi_bar, 128);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -525,6 +536,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
     const int et = threadIdx.x - 128;                 // TMEM lane 0..127
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t au = 0;
+    uint32_t eph = 0;   // phase of epi_bar
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit U = get_unit<EPI, BT>(p, u);
       const int nch = (U.rows + 31) >> 5;
@@ -550,7 +562,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
           float* sa = sAs + (kb & 1) * BT;
           if (et < BT) sa[et] = as_nx;
           const float ws = ws_nx;
-          named_bar_sync(1, 128);
+          if (!group_sync(epi_bar, eph, wc)) goto epi_done;
           if (kb + 1 < U.kb1) {
             as_nx = as_at(kb + 1);
             ws_nx = ws_at(kb + 1);
@@ -602,7 +614,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
           if (c < nch) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) sOut[j * 128 + et] = acc[c * 32 + j] * fscale;
-            named_bar_sync(1, 128);
+            if (!group_sync(epi_bar, eph, wc)) goto epi_done;
             if (EPI == EPI_DENSE) {
               const int nl = (et & 31) * 4;
               const int n = U.n0 + nl;
@@ -679,7 +691,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
                   if (n + i < p.N) dst[n + i] = (vv[i] + load_bias(p, U.e * p.bias_e + n + i)) * rw;
               }
             }
-            named_bar_sync(1, 128);
+            if (!group_sync(epi_bar, eph, wc)) goto epi_done;
           }
         }
       }

@@ -1,0 +1,205 @@
+"""fp8_scaled_mm on the GPU vs the oracle.
+
+W8A8 block (both weight block shapes) and W8A16 per-tensor at sizes that span
+several tiles and ragged tails, the per-tensor == constant-block identity,
+the scale-layout bit-identity, split-K, and the full-size block workloads
+(sampled full rows)."""
+import numpy as np
+import pytest
+import torch
+
+import mxfp4_quantized_gemm_token_gb300 as mxq
+from mxfp4_quantized_gemm_token_gb300 import _lib, synth
+from gpu_util import assert_bf16_close, assert_probe_close, bits16, u8
+
+pytestmark = pytest.mark.gpu
+E4M3, BF16 = 3, 1
+
+
+def block_case(oracle, M, N, K, block_n, seed, bias=None, x=None):
+    if x is None:
+        x = synth.activations(M, K, seed=seed)
+    wq, ws = synth.block_fp8_weight(N, K, block_n, seed=seed + 1)
+    rq, rs = oracle.per_token_group_quant_fp8(bits16(x), 128)
+    b_np = None if bias is None else (bits16(bias) if bias.dtype == torch.bfloat16 else bias.numpy())
+    rf, rb = oracle.scaled_mm(rq, E4M3, rs, u8(wq), ws.numpy(), block_n, 128, b_np)
+    xc = x.cuda()
+    q, s = mxq.per_token_group_quant_fp8(xc)
+    bc = None if bias is None else bias.cuda()
+    o32 = mxq.fp8_scaled_mm(q, wq.cuda(), ws.cuda(), [block_n, 128], a_scale=s, bias=bc,
+                            out_dtype=torch.float32)
+    o16 = mxq.fp8_scaled_mm(q, wq.cuda(), ws.cuda(), [block_n, 128], a_scale=s, bias=bc)
+    torch.cuda.synchronize()
+    assert_probe_close(o32, rf)
+    assert_bf16_close(o16, rb)
+    return o32, o16
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (17, 384, 896), (97, 200, 640),
+                                   (130, 256, 384), (64, 128, 128), (33, 640, 1024),
+                                   (300, 384, 256)])
+def test_w8a8_block128(oracle, M, N, K):
+    bias = torch.randn(N, generator=torch.Generator().manual_seed(M))
+    block_case(oracle, M, N, K, 128, seed=M + N, bias=bias)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 256, 256), (65, 300, 512), (2, 4096, 1024)])
+def test_w8a8_block1x128(oracle, M, N, K):
+    block_case(oracle, M, N, K, 1, seed=M * 3 + 1)
+
+
+def test_w8a8_page_numerical_case_bf16_bias(oracle):
+    """The XPU page's numerical test shape: M, K, N = 16, 256, 256, block
+    [128, 128], weight_scale = rand + 0.1, bf16 bias."""
+    g = torch.Generator().manual_seed(0)
+    x = torch.randn(16, 256, generator=g).to(torch.bfloat16)
+    w = torch.randn(256, 256, generator=g).to(torch.float8_e4m3fn)
+    ws = torch.rand(2, 2, generator=g) + 0.1
+    bias = torch.randn(256, generator=g).to(torch.bfloat16)
+    rq, rs = oracle.per_token_group_quant_fp8(bits16(x), 128)
+    rf, rb = oracle.scaled_mm(rq, E4M3, rs, u8(w), ws.numpy(), 128, 128, bits16(bias))
+    out = mxq.w8a8_block_fp8_linear(x.cuda(), w.cuda(), [128, 128], ws.cuda(), bias=bias.cuda())
+    assert out.dtype == torch.bfloat16
+    assert_bf16_close(out, rb)
+    # post-load transposed-contiguous scale storage: bit-identical output
+    ws_t = torch.empty_strided(ws.shape, (1, ws.shape[0]), device="cuda")
+    ws_t.copy_(ws.cuda())
+    out_t = mxq.w8a8_block_fp8_linear(x.cuda(), w.cuda(), [128, 128], ws_t, bias=bias.cuda())
+    assert torch.equal(out, out_t)
+    # pre-quantized input path returns bf16 as well
+    q, s = mxq.per_token_group_quant_fp8(x.cuda())
+    out_q = mxq.w8a8_block_fp8_linear(q, w.cuda(), [128, 128], ws.cuda(), input_scale=s,
+                                      bias=bias.cuda())
+    assert out_q.dtype == torch.bfloat16 and torch.equal(out_q, out)
+
+
+def test_linear_rejects_mxfp8_block():
+    x = torch.zeros(4, 256, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(128, 256, dtype=torch.float8_e4m3fn, device="cuda")
+    with pytest.raises(ValueError):
+        mxq.w8a8_block_fp8_linear(x, w, [1, 32], torch.ones(128, 8, device="cuda"))
+    with pytest.raises(mxq.MxqError) as ei:
+        q, s = mxq.per_token_group_quant_fp8(x)
+        mxq.fp8_scaled_mm(q, w, torch.ones(128, 8, device="cuda"), [1, 32], a_scale=s)
+    assert ei.value.status == _lib.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("M", [1, 11, 97])
+@pytest.mark.parametrize("N", [128, 224])
+@pytest.mark.parametrize("K", [512, 576])
+@pytest.mark.parametrize("has_bias", [False, True])
+def test_w8a16_per_tensor_page_grid(oracle, M, N, K, has_bias):
+    a, w, scale, bias = synth.per_tensor_fp8_problem(M=M, N=N, K=K, seed=M + N + K, bias=has_bias)
+    rf, rb = oracle.scaled_mm(bits16(a), BF16, None, u8(w), scale.numpy(), 0, 0,
+                              None if bias is None else bias.numpy())
+    bc = None if bias is None else bias.cuda()
+    for sc in (scale.cuda(), scale.reshape(1).cuda()):        # 0-d and [1] scales
+        o16 = mxq.fp8_scaled_mm(a.cuda(), w.cuda(), sc, None, bias=bc)
+        o32 = mxq.fp8_scaled_mm(a.cuda(), w.cuda(), sc, None, bias=bc, out_dtype=torch.float32)
+        assert_bf16_close(o16, rb)
+        assert_probe_close(o32, rf)
+
+
+def test_w8a16_per_tensor_config(oracle):
+    """The per-tensor W8A16 workload: A [97, 576], B [224, 576], scale 0.01, bias."""
+    a, w, scale, bias = synth.per_tensor_fp8_problem(seed=0)
+    rf, rb = oracle.scaled_mm(bits16(a), BF16, None, u8(w), scale.numpy(), 0, 0, bias.numpy())
+    o16 = mxq.fp8_per_tensor_linear(a.cuda(), w.cuda(), scale.cuda(), bias.cuda())
+    assert_bf16_close(o16, rb)
+
+
+def test_per_tensor_equals_constant_blocks_on_gpu():
+    a, w, scale, bias = synth.per_tensor_fp8_problem(M=40, N=256, K=512, seed=3)
+    ac, wc = a.cuda(), w.cuda()
+    pt = mxq.fp8_scaled_mm(ac, wc, scale.cuda(), None, out_dtype=torch.float32)
+    blk = mxq.fp8_scaled_mm(ac, wc, torch.full((2, 4), 0.01, device="cuda"), [128, 128],
+                            out_dtype=torch.float32)
+    assert_probe_close(blk, pt.double().cpu().numpy())
+
+
+def test_w8a16_with_block_weights(oracle):
+    M, N, K = 20, 256, 384
+    a = synth.activations(M, K, seed=4)
+    wq, ws = synth.block_fp8_weight(N, K, 128, seed=5)
+    rf, rb = oracle.scaled_mm(bits16(a), BF16, None, u8(wq), ws.numpy(), 128, 128)
+    o = mxq.fp8_scaled_mm(a.cuda(), wq.cuda(), ws.cuda(), [128, 128], out_dtype=torch.float32)
+    assert_probe_close(o, rf)
+
+
+def test_split_k_matches(oracle):
+    M, N, K = 8, 256, 2048
+    x = synth.activations(M, K, seed=21)
+    wq, ws = synth.block_fp8_weight(N, K, 128, seed=22)
+    rq, rs = oracle.per_token_group_quant_fp8(bits16(x), 128)
+    rf, _ = oracle.scaled_mm(rq, E4M3, rs, u8(wq), ws.numpy(), 128, 128)
+    q, s = mxq.per_token_group_quant_fp8(x.cuda())
+    try:
+        for sp in (2, 3, 16):
+            mxq.set_option(_lib.OPT_SPLIT_K, sp)
+            o = mxq.fp8_scaled_mm(q, wq.cuda(), ws.cuda(), [128, 128], a_scale=s,
+                                  out_dtype=torch.float32)
+            assert_probe_close(o, rf, what="split %d" % sp)
+    finally:
+        mxq.set_option(_lib.OPT_SPLIT_K, 0)
+
+
+def test_persistent_loop_several_units_per_cta(oracle):
+    """Cap the grid at 3 CTAs so each CTA runs many tiles back to back."""
+    try:
+        mxq.set_option(_lib.OPT_NUM_SMS, 3)
+        block_case(oracle, 150, 520, 512, 128, seed=31)
+        a, w, scale, bias = synth.per_tensor_fp8_problem(M=97, N=600, K=576, seed=32)
+        rf, rb = oracle.scaled_mm(bits16(a), BF16, None, u8(w), scale.numpy(), 0, 0, bias.numpy())
+        o = mxq.fp8_scaled_mm(a.cuda(), w.cuda(), scale.cuda(), None, bias=bias.cuda())
+        assert_bf16_close(o, rb)
+    finally:
+        mxq.set_option(_lib.OPT_NUM_SMS, 0)
+
+
+def test_empty_problems_are_noops():
+    w = torch.zeros(128, 256, dtype=torch.float8_e4m3fn, device="cuda")
+    a = torch.zeros(0, 256, dtype=torch.bfloat16, device="cuda")
+    out = mxq.fp8_scaled_mm(a, w, torch.tensor(1.0, device="cuda"), None)
+    assert out.shape == (0, 128)
+
+
+# ------------------------------------------------------------ full size
+
+@pytest.fixture(scope="module")
+def big_w128():
+    wq, ws = synth.block_fp8_weight(18432, 7168, 128, seed=0, device="cuda")
+    return wq, ws, u8(wq), ws.cpu().numpy()
+
+
+@pytest.mark.parametrize("M", [1, 8, 17, 128, 1024, 4096])
+def test_full_size_block128_sampled_rows(oracle, big_w128, M):
+    wq, ws, w_np, ws_np = big_w128
+    x = synth.activations(M, 7168, seed=100 + M, device="cuda")
+    q, s = mxq.per_token_group_quant_fp8(x)
+    o32 = mxq.fp8_scaled_mm(q, wq, ws, [128, 128], a_scale=s, out_dtype=torch.float32)
+    o16 = mxq.fp8_scaled_mm(q, wq, ws, [128, 128], a_scale=s)
+    rows = sorted(set([0, M - 1, M // 2, (M * 7) // 11]))
+    ridx = torch.tensor(rows, device="cuda")
+    rq, rs = oracle.per_token_group_quant_fp8(bits16(x[ridx]), 128)
+    rf, rb = oracle.scaled_mm(rq, E4M3, rs, w_np, ws_np, 128, 128)
+    assert_probe_close(o32[ridx], rf)
+    assert_bf16_close(o16[ridx], rb)
+
+
+@pytest.mark.parametrize("M", [1, 64, 2048])
+def test_full_size_block1x128_sampled_rows(oracle, M):
+    wq, ws = synth.block_fp8_weight(4096, 7168, 1, seed=1, device="cuda")
+    if M >= 64:
+        base = synth.activations(M, 7168 + 128, seed=200 + M, device="cuda").view(2, M // 2, 7296)
+        x = base[:, :, :7168]                       # non-contiguous 3-D input
+    else:
+        x = synth.activations(M, 7168, seed=200 + M, device="cuda")
+    out = mxq.w8a8_block_fp8_linear(x, wq, [1, 128], ws)
+    assert out.shape == (*x.shape[:-1], 4096)
+    flat = out.reshape(-1, 4096)
+    xf = x.reshape(-1, 7168)
+    rows = sorted(set([0, M - 1, M // 3]))
+    ridx = torch.tensor(rows, device="cuda")
+    rq, rs = oracle.per_token_group_quant_fp8(bits16(xf[ridx]), 128)
+    _, rb = oracle.scaled_mm(rq, E4M3, rs, u8(wq), ws.cpu().numpy(), 1, 128)
+    assert_bf16_close(flat[ridx], rb)

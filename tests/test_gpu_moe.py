@@ -1,0 +1,131 @@
+"""moe_align_block and fused_experts on the GPU vs the oracle.
+
+Alignment is bit-exact; the fused MoE output is compared after bf16 rounding
+(rtol = atol = 1e-2), with its checkpoints (act, y) as well.  Covers both
+weight formats, biases, ragged K / N tails, empty experts and the expert block
+sizes 4 / 5 / 33, topk > 1, every block_m, and both instruction-width paths."""
+import numpy as np
+import pytest
+import torch
+
+import mxfp4_quantized_gemm_token_gb300 as mxq
+from mxfp4_quantized_gemm_token_gb300 import _lib, synth
+from gpu_util import assert_bf16_close, bits16, u8
+
+pytestmark = pytest.mark.gpu
+W_FP8, W_MX = 1, 2
+
+
+# ------------------------------------------------------------- align
+
+@pytest.mark.parametrize("T,topk,E,BM,kind", [
+    (1, 4, 128, 16, "uniform"), (37, 8, 256, 64, "uniform"), (64, 4, 128, 32, "zipf"),
+    (300, 8, 256, 128, "zipf"), (5, 2, 3, 16, "uniform"), (1024, 8, 256, 64, "uniform"),
+    (4096, 8, 256, 128, "zipf")])
+def test_align_bit_exact(oracle, T, topk, E, BM, kind):
+    fn = synth.routing_uniform if kind == "uniform" else synth.routing_zipf
+    _, ids = fn(T, E, topk, seed=T + E)
+    ref = oracle.moe_align(ids.numpy(), E, BM)
+    got = mxq.moe_align_block(ids.cuda(), E, BM)
+    for r, g in zip(ref[:3], got[:3]):
+        assert np.array_equal(r, g.cpu().numpy())
+    assert int(got[3].item()) == ref[3]
+
+
+def test_align_small_blocks_and_empty_experts(oracle):
+    _, ids = synth.routing_blocks((0, 4, 5, 33), topk=8, E=256)
+    for BM in (16, 32, 64, 128):
+        ref = oracle.moe_align(ids.numpy(), 256, BM)
+        got = mxq.moe_align_block(ids.cuda(), 256, BM)
+        for r, g in zip(ref[:3], got[:3]):
+            assert np.array_equal(r, g.cpu().numpy())
+
+
+def test_align_flags_out_of_range_ids():
+    ids = torch.tensor([[0, 1], [7, 2]], dtype=torch.int32, device="cuda")
+    mxq.moe_align_block(ids, 4, 16)
+    with pytest.raises(mxq.MxqError) as ei:
+        mxq.sync_status()
+    assert ei.value.status == _lib.ERR_DEVICE
+    mxq.sync_status()          # the word was cleared
+
+
+# ------------------------------------------------------------ fused MoE
+
+def weights(wtype, E, N, K, seed, bias):
+    if wtype == W_FP8:
+        w1, s1, w2, s2 = synth.moe_fp8_weights(E, N, K, seed=seed)
+    else:
+        w1, s1, w2, s2 = synth.moe_mxfp4_weights(E, N, K, seed=seed)
+    b1 = b2 = None
+    if bias:
+        b1, b2 = synth.moe_biases(E, N, K, seed=seed + 1)
+    return w1, s1, w2, s2, b1, b2
+
+
+def run_moe(oracle, wtype, E, N, K, x, tw, ids, block_m, seed=1, bias=False, check_ckpt=True):
+    w1, s1, w2, s2, b1, b2 = weights(wtype, E, N, K, seed, bias)
+    sc = (lambda s: u8(s)) if wtype == W_MX else (lambda s: s.numpy())
+    ref, ract, rz = oracle.fused_experts(
+        bits16(x), wtype, u8(w1), sc(s1), None if b1 is None else b1.numpy(), u8(w2), sc(s2),
+        None if b2 is None else b2.numpy(), tw.numpy(), ids.numpy(), N, checkpoints=True)
+    cu = lambda t: None if t is None else t.cuda()
+    out, act, y = mxq.fused_experts(cu(x), cu(w1), cu(s1), cu(w2), cu(s2), cu(tw), cu(ids),
+                                    wtype=wtype, w1_bias=cu(b1), w2_bias=cu(b2),
+                                    block_m=block_m, checkpoints=True)
+    mxq.sync_status()
+    assert_bf16_close(out, ref, what="moe output")
+    if check_ckpt:
+        assert_bf16_close(act, ract, what="act checkpoint")
+        yref = rz * tw.numpy().reshape(-1, 1).astype(np.float64)
+        scale = np.abs(yref).max(axis=1, keepdims=True)
+        assert np.all(np.abs(y.double().cpu().numpy() - yref) <= 2e-2 * (np.abs(yref) + 0.05 * scale))
+    return out
+
+
+@pytest.mark.parametrize("block_m", [16, 32, 64, 128])
+def test_fused_fp8_small(oracle, block_m):
+    E, N, K, T, topk = 8, 128, 256, 13, 2
+    x = synth.activations(T, K, seed=3, scale_div=10)
+    tw, ids = synth.routing_uniform(T, E, topk, seed=4)
+    run_moe(oracle, W_FP8, E, N, K, x, tw, ids, block_m)
+
+
+def test_fused_fp8_ragged_dims_and_many_tokens(oracle):
+    E, N, K, T, topk = 6, 192, 400, 70, 3       # K, N not multiples of 128
+    x = synth.activations(T, K, seed=5, scale_div=10)
+    tw, ids = synth.routing_zipf(T, E, topk, seed=6)
+    run_moe(oracle, W_FP8, E, N, K, x, tw, ids, 32)
+
+
+@pytest.mark.parametrize("block_m", [16, 64])
+def test_fused_mxfp4_bias(oracle, block_m):
+    E, N, K, T, topk = 4, 160, 288, 9, 4
+    x = synth.activations(T, K, seed=7, scale_div=10)
+    tw, ids = synth.routing_uniform(T, E, topk, seed=8)
+    run_moe(oracle, W_MX, E, N, K, x, tw, ids, block_m, bias=True)
+
+
+@pytest.mark.parametrize("topk", [1, 8])
+def test_fused_small_expert_blocks_4_5_33(oracle, topk):
+    """Expert blocks of exactly 0, 4, 5 and 33 tokens (the vLLM CPU page's
+    small-block test, plus topk > 1 and N != K which it left out)."""
+    E = 256 if topk == 8 else 8
+    tw, ids = synth.routing_blocks((0, 4, 5, 33), topk=topk, E=E)
+    T = ids.shape[0]
+    N, K = 128, 256
+    x = synth.activations(T, K, seed=9, scale_div=10)
+    run_moe(oracle, W_FP8, E, N, K, x, tw, ids, 16, check_ckpt=(topk == 1))
+
+
+def test_fused_narrow_and_wide_paths_agree(oracle):
+    E, N, K, T, topk = 8, 128, 256, 21, 2
+    x = synth.activations(T, K, seed=11, scale_div=10)
+    tw, ids = synth.routing_zipf(T, E, topk, seed=12)
+    try:
+        for force in (1, 2):
+            mxq.set_option(_lib.OPT_FORCE_PATH, force)
+            run_moe(oracle, W_FP8, E, N, K, x, tw, ids, 64)
+            run_moe(oracle, W_MX, E, N, K, x, tw, ids, 64)
+    finally:
+        mxq.set_option(_lib.OPT_FORCE_PATH, 0)
