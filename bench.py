@@ -1,0 +1,358 @@
+"""Benchmark of the quantized scaled-GEMM hot path on GB300.
+
+Default workload (one "step"): the block-FP8 W8A8 linear with weight blocks
+[128, 128], W e4m3 [18432, 7168], for a batch of activations at every token
+count M in {1, 8, 17, 128, 1024, 4096}: per M, per-token-group quantization
+of the bf16 activations followed by the scaled GEMM.  The metric is the
+whole-job throughput in TFLOP/s (2*M*N*K summed over the six GEMMs, divided
+by the step time).  Inputs are seeded synthetic data; every GEMM of a step
+reads its own copy of W (6 distinct 132 MB copies), so no GEMM finds its
+weights in the 129 MB L2.
+
+Other workloads (--workload) measure the remaining hot-path configurations
+for the tables in the design doc; the default line is the contract line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+N_W, K_W = 18432, 7168
+M_SET = (1, 8, 17, 128, 1024, 4096)
+METRIC = "FP8 block-scaled W8A8 linear (quant + scaled GEMM) throughput, [128,128] weights"
+WORKLOAD = ("block-FP8 W8A8 linear, W e4m3 [18432, 7168] with [128,128] fp32 block scales, "
+            "bf16 activations M in {1,8,17,128,1024,4096} quantized per 1x128 group")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class Clocks:
+    """Samples nvidia-smi during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            p = [x.strip() for x in l.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------- workloads
+
+def make_block128_inputs(dev, seed_base=0):
+    from mxfp4_quantized_gemm_token_gb300 import synth
+    ws_list = [synth.block_fp8_weight(N_W, K_W, 128, seed=seed_base + i, device=dev)
+               for i in range(len(M_SET))]
+    xs = [synth.activations(M, K_W, seed=1000 + M, device=dev) for M in M_SET]
+    return ws_list, xs
+
+
+def step_block128(mxq, ws_list, xs, outs, workspaces, dom_events=None):
+    for i, M in enumerate(M_SET):
+        wq, wsc = ws_list[i]
+        q, s = mxq.per_token_group_quant_fp8(xs[i])
+        if dom_events is not None and M == M_SET[-1]:
+            dom_events[0].record()
+        outs[i] = mxq.fp8_scaled_mm(q, wq, wsc, [128, 128], a_scale=s, workspace=workspaces[i])
+        if dom_events is not None and M == M_SET[-1]:
+            dom_events[1].record()
+
+
+def flops_block128():
+    return sum(2.0 * M * N_W * K_W for M in M_SET)
+
+
+_ORACLE_INPUTS = []
+
+
+def cpu_oracle_sample(seconds: float = 12.0, max_rows: int = 64):
+    """The oracle (plain C, fp64) on a bounded sample of the default workload:
+    whole rows of the M = 4096 GEMM (activation quantization + all 18432
+    outputs of each row), rows added until the time budget is spent."""
+    import oracle
+    oracle.build()
+    if not _ORACLE_INPUTS:
+        from mxfp4_quantized_gemm_token_gb300 import synth
+        wq, ws = synth.block_fp8_weight(N_W, K_W, 128, seed=0)
+        x = synth.activations(64, K_W, seed=1000 + 4096)
+        _ORACLE_INPUTS.extend([wq.view(torch.uint8).numpy(), ws.numpy(),
+                               x.view(torch.int16).numpy().view(np.uint16)])
+    w_np, ws_np, xb = _ORACLE_INPUTS
+    rows, t_total = 0, 0.0
+    while rows < max_rows and t_total < seconds:
+        t0 = time.perf_counter()
+        q, s = oracle.per_token_group_quant_fp8(xb[rows:rows + 1], 128)
+        oracle.scaled_mm(q, oracle.E4M3, s, w_np, ws_np, 128, 128)
+        t_total += time.perf_counter() - t0
+        rows += 1
+    flops = 2.0 * rows * N_W * K_W
+    return {"value": flops / t_total / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": "%d full rows (quant + 18432 outputs each) of the M=4096 GEMM, %.1f s"
+                      % (rows, t_total)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    steps = []
+    for _ in range(args.warmup):
+        cpu_oracle_sample(seconds=2.0, max_rows=2)
+    t0 = time.perf_counter()
+    res = None
+    for _ in range(args.steps):
+        res = cpu_oracle_sample(seconds=max(3.0, 20.0 / max(1, args.steps)), max_rows=64)
+        steps.append(res["value"])
+    elapsed = time.perf_counter() - t0
+    v = statistics.mean(steps)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * elapsed / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": res["sample"] if res else None},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": res["cores"] if res else None,
+                             "kind": "oracle", "sample": res["sample"] if res else None},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args, world, rank, local):
+    import mxfp4_quantized_gemm_token_gb300 as mxq
+    dev = torch.device("cuda", local)
+    pk, pk_src = peaks()
+    ws_list, xs = make_block128_inputs(dev)
+    outs = [None] * len(M_SET)
+    workspaces = []
+    launches_per_step = 0
+    import ctypes
+    lib = mxq._lib.load()
+    for M in M_SET:
+        sz = ctypes.c_size_t(0)
+        mxq.check(lib.mxq_fp8_scaled_mm_workspace_size(M, N_W, K_W, 3, ctypes.byref(sz)))
+        workspaces.append(torch.empty(sz.value, dtype=torch.uint8, device=dev) if sz.value else None)
+        launches_per_step += 2 + (1 if sz.value else 0)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step_block128(mxq, ws_list, xs, outs, workspaces)
+    mxq.sync_status(dev)
+    torch.cuda.synchronize()
+
+    dom = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        start.record()
+        for k in range(args.steps):
+            step_block128(mxq, ws_list, xs, outs, workspaces, dom_events=dom[k])
+        end.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = max_over_ranks(world, start.elapsed_time(end))
+    mxq.sync_status(dev)
+    ms_step = ms_total / args.steps
+    flops = flops_block128()
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    dom_ms = statistics.mean(a.elapsed_time(b) for a, b in dom)
+    dom_flops = 2.0 * M_SET[-1] * N_W * K_W
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    fp8_peak = 2.0 * pk["bf16_tflops"]          # e4m3 = 2 x bf16 (nominal ratio 4.5 / 2.25)
+
+    # ---- end to end: host activations in, host outputs back, through the API
+    pinned_in = [x.cpu().pin_memory() for x in xs]
+    pinned_out = [torch.empty((M, N_W), dtype=torch.bfloat16).pin_memory() for M in M_SET]
+    h2d = sum(t.numel() * t.element_size() for t in pinned_in)
+    d2h = sum(t.numel() * t.element_size() for t in pinned_out)
+    dev_in = [torch.empty_like(x) for x in xs]
+
+    def e2e_step():
+        for i, M in enumerate(M_SET):
+            dev_in[i].copy_(pinned_in[i], non_blocking=True)
+            q, s = mxq.per_token_group_quant_fp8(dev_in[i])
+            o = mxq.fp8_scaled_mm(q, ws_list[i][0], ws_list[i][1], [128, 128], a_scale=s,
+                                  workspace=workspaces[i])
+            pinned_out[i].copy_(o, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1)) / args.steps
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 x fp8_e4m3 -> f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": list(M_SET), "N": N_W, "K": K_W,
+                   "weight_block": [128, 128], "activation_group": 128,
+                   "l2": "6 distinct 132 MB weight copies, one per GEMM of a step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": None,
+                     "kernel": "gemm_kernel<F8F8,DENSE,128,promote> at M=4096",
+                     "peak_source": "%s bf16 burst %.1f TFLOP/s x 2 (e4m3/bf16 nominal)"
+                                    % (pk_src, pk["bf16_tflops"]),
+                     "launch_ms": dom_ms},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if args.traffic is not None:
+        line["roofline"]["traffic"] = args.traffic
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_profile(args, local):
+    """A few launches of one shape (for ncu captures): quant + GEMM at M."""
+    import mxfp4_quantized_gemm_token_gb300 as mxq
+    from mxfp4_quantized_gemm_token_gb300 import synth
+    dev = torch.device("cuda", local)
+    M = args.profile
+    wq, wsc = synth.block_fp8_weight(N_W, K_W, 128, seed=0, device=dev)
+    x = synth.activations(M, K_W, seed=1000 + M, device=dev)
+    for _ in range(3):
+        q, s = mxq.per_token_group_quant_fp8(x)
+        out = mxq.fp8_scaled_mm(q, wq, wsc, [128, 128], a_scale=s)
+    torch.cuda.synchronize()
+    mxq.sync_status(dev)
+    print(json.dumps({"profile_M": M, "checksum": float(out.float().abs().sum().item())}))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mxq", choices=["mxq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", type=int, default=0,
+                    help="run 3 launches of quant + GEMM at this M only (for ncu)")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu DRAM bytes per launch of the dominant kernel (if measured)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    if args.profile:
+        return run_profile(args, local)
+    return run_gpu(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
