@@ -136,6 +136,36 @@ mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t M, int64_t 
                              int32_t bias_dtype, void* out, int32_t out_dtype, int64_t ldo,
                              void* workspace, size_t ws_bytes, mxq_stream_t stream);
 
+/*
+ * mxq_fp8_scaled_mm for callers that cannot allocate device memory (no
+ * counterpart on the pages; it exists for this library's users).  Some callers
+ * cannot call cudaMalloc or hand over a workspace: plugins that receive only
+ * their input and output buffers, code inside a framework whose memory pool
+ * forbids raw allocations, or serving loops that must not allocate after
+ * start-up.  This entry point takes exactly the arguments of mxq_fp8_scaled_mm
+ * minus the workspace and computes the same result; the split-K partial sums
+ * it needs live in one fixed array inside the library,
+ * MXQ_NOALLOC_SCRATCH_BYTES (16 MiB) per GPU, held from library load until the
+ * process exits.  It allocates nothing.
+ *   - A shape whose split-K plan needs more scratch than that is rejected with
+ *     MXQ_ERR_UNSUPPORTED (mxq_last_error says how much it needs); shapes that
+ *     need no split (large M) need no scratch and are always accepted.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array and its contents are left
+ *     from the previous call (the partials are fully rewritten, so nothing
+ *     needs to start at zero).  Calls whose executions overlap on the GPU,
+ *     e.g. on two streams at once, race on the array: serialize them.
+ */
+#define MXQ_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+mxq_status mxq_fp8_scaled_mm_noalloc(const void* A, int32_t a_dtype, int64_t M, int64_t K,
+                                     int64_t lda, const float* a_scale, int64_t sa0, int64_t sa1,
+                                     const void* W, int64_t N, int64_t ldw, const float* w_scale,
+                                     int32_t block_n, int32_t block_k, int64_t sw0, int64_t sw1,
+                                     const void* bias, int32_t bias_dtype, void* out,
+                                     int32_t out_dtype, int64_t ldo, mxq_stream_t stream);
+
 /* Workspace bytes that let mxq_fp8_scaled_mm use its preferred split-K plan
  * for this shape on the current device (0 when no split is needed). */
 mxq_status mxq_fp8_scaled_mm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t a_dtype,

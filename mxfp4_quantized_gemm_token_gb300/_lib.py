@@ -26,8 +26,10 @@ EXPORTED = [
     "mxq_last_error", "mxq_version", "mxq_set_option", "mxq_get_option", "mxq_sync_status",
     "mxq_per_token_group_quant_fp8", "mxq_fp8_scaled_mm", "mxq_fp8_scaled_mm_workspace_size",
     "mxq_moe_align_block", "mxq_fused_experts", "mxq_fused_experts_debug",
-    "mxq_fused_experts_workspace_size",
+    "mxq_fused_experts_workspace_size", "mxq_fp8_scaled_mm_noalloc",
 ]
+
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class MxqError(RuntimeError):
@@ -49,6 +51,8 @@ def _declare(lib):
         "mxq_per_token_group_quant_fp8": (st, [P, I64, I64, I64, I32, F, P, P, P]),
         "mxq_fp8_scaled_mm": (st, [P, I32, I64, I64, I64, P, I64, I64, P, I64, I64, P, I32, I32,
                                    I64, I64, P, I32, P, I32, I64, P, SZ, P]),
+        "mxq_fp8_scaled_mm_noalloc": (st, [P, I32, I64, I64, I64, P, I64, I64, P, I64, I64, P,
+                                           I32, I32, I64, I64, P, I32, P, I32, I64, P]),
         "mxq_fp8_scaled_mm_workspace_size": (st, [I64, I64, I64, I32, ctypes.POINTER(SZ)]),
         "mxq_moe_align_block": (st, [P, I64, I32, I32, I32, P, P, P, P, I64, P, SZ, P]),
         "mxq_fused_experts": (st, [P, I64, I64, I64, I32, I32, I64, P, P, P, P, P, P, P, P, I32,

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmxq.so")
 
-SOURCES = ["api.cu", "quant.cu", "moe_aux.cu", "gemm_dense.cu", "gemm_moe.cu"]
+SOURCES = ["api.cu", "quant.cu", "moe_aux.cu", "gemm_dense.cu", "gemm_moe.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

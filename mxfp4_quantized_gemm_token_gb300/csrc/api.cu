@@ -45,6 +45,8 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace
 
+void set_last_error(const std::string& msg) { g_err = msg; }
+
 int64_t option(int32_t which) {
   if (which < 0 || which >= 8) return 0;
   return g_opts[which].load();

@@ -21,6 +21,9 @@ struct DeviceInfo {
 // Per-device facts, checked once per device (compute capability 10.3).
 bool device_info(DeviceInfo* info, std::string* err);
 
+// Sets the message mxq_last_error() returns on this thread.
+void set_last_error(const std::string& msg);
+
 // Process-wide options (see MXQ_OPT_*).
 int64_t option(int32_t which);
 
