@@ -74,7 +74,9 @@ enum {
   MXQ_OPT_SPLIT_K = 4,      /* fp8_scaled_mm split-K: 0 auto, else the factor */
   MXQ_OPT_INJECT_STALL = 5, /* TEST ONLY: GEMM producers issue no copy, so every
                                consumer wait runs out (exercises MXQ_ERR_TIMEOUT) */
-  MXQ_OPT_NUM_SMS = 6       /* persistent grid size cap; 0 = all SMs */
+  MXQ_OPT_NUM_SMS = 6,      /* persistent grid size cap; 0 = all SMs */
+  MXQ_OPT_TILE_N = 7        /* fp8_scaled_mm token-tile width: 0 auto, or 32, 64, 128,
+                               256 (256 for FP8 activations only) */
 };
 
 const char* mxq_last_error(void);

@@ -19,8 +19,8 @@ _lib = None
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(6)
 BF16, F32, E4M3, E2M1X2, UE8M0 = 1, 2, 3, 4, 5
 W_FP8_BLOCK128, W_MXFP4 = 1, 2
-OPT_SMALL_M_MAX, OPT_FORCE_PATH, OPT_WAIT_BUDGET_NS, OPT_SPLIT_K, OPT_INJECT_STALL, OPT_NUM_SMS = (
-    1, 2, 3, 4, 5, 6)
+(OPT_SMALL_M_MAX, OPT_FORCE_PATH, OPT_WAIT_BUDGET_NS, OPT_SPLIT_K, OPT_INJECT_STALL, OPT_NUM_SMS,
+ OPT_TILE_N) = (1, 2, 3, 4, 5, 6, 7)
 
 EXPORTED = [
     "mxq_last_error", "mxq_version", "mxq_set_option", "mxq_get_option", "mxq_sync_status",

@@ -132,8 +132,11 @@ extern "C" const char* mxq_last_error(void) { return g_err.c_str(); }
 extern "C" const char* mxq_version(void) { return "mxq 0.1 (sm_103a, tcgen05)"; }
 
 extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
-  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_NUM_SMS)
+  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_TILE_N)
     return fail(MXQ_ERR_INVALID_ARG, "unknown option " + std::to_string(opt));
+  if (opt == MXQ_OPT_TILE_N && value != 0 && value != 32 && value != 64 && value != 128 &&
+      value != 256)
+    return fail(MXQ_ERR_INVALID_ARG, "TILE_N is 0 (auto), 32, 64, 128 or 256");
   if (value < 0) return fail(MXQ_ERR_INVALID_ARG, "option values are non-negative");
   if (opt == MXQ_OPT_FORCE_PATH && value > 2)
     return fail(MXQ_ERR_INVALID_ARG, "FORCE_PATH is 0 (auto), 1 (narrow) or 2 (full width)");
@@ -142,7 +145,7 @@ extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
 }
 
 extern "C" mxq_status mxq_get_option(int32_t opt, int64_t* value) {
-  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_NUM_SMS || value == nullptr)
+  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_TILE_N || value == nullptr)
     return fail(MXQ_ERR_INVALID_ARG, "unknown option or NULL value");
   *value = g_opts[opt].load();
   return MXQ_OK;
@@ -206,8 +209,10 @@ struct MmPlan {
 MmPlan plan_mm(int64_t M, int64_t N, int64_t K, int32_t a_dtype, bool block, bool has_ascale,
                int num_sms) {
   MmPlan pl;
-  pl.bt = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
   pl.kind = a_dtype == MXQ_E4M3 ? KIND_F8F8 : KIND_F8W;
+  pl.bt = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
+  const int64_t tile = option(MXQ_OPT_TILE_N);
+  if (tile > 0) pl.bt = (tile == 256 && pl.kind != KIND_F8F8) ? 128 : static_cast<int>(tile);
   pl.promote = block || has_ascale;
   pl.tiles_n = static_cast<int>(cdiv(N, 128));
   pl.tiles_m = static_cast<int>(cdiv(M, pl.bt));
@@ -305,7 +310,7 @@ extern "C" mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t 
   if (!make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, K, N, ldw, 128, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B, &err))
     return fail(MXQ_ERR_CUDA, err);
-  const int bv = pl.bt == 32 ? 1 : (pl.bt == 64 ? 2 : 3);
+  const int bv = pl.bt == 32 ? 1 : (pl.bt == 64 ? 2 : (pl.bt == 128 ? 3 : 4));
   if (a_dtype == MXQ_E4M3) {
     if (!make_map_2d(&maps.b[bv], CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, lda, 128, pl.bt,
                      CU_TENSOR_MAP_SWIZZLE_128B, &err))

@@ -11,8 +11,13 @@
 //   warp 0        TMA producer for the weight operand (A ring)
 //   warp 1        TMEM allocator + single-thread tcgen05.mma issuer
 //   warp 2        TMA producer for the token operand (B ring)
-//   warps 4..7    epilogue: TMEM -> registers, scale promotion, output
-//   warps 8..11   (bf16 kinds only) in-shared-memory weight decode
+//   warp 3        scale loader: per 128-wide K slice, the column scales
+//                 As(m, kb) (times the tile's Ws(kb) when it is uniform) and,
+//                 when it is not, the per-row Ws(n, kb), into a shared ring
+//   warps 4..     epilogue, one or two warpgroups splitting the token columns:
+//                 TMEM -> registers, scale promotion (one FFMA per element),
+//                 output
+//   last 4 warps  (bf16 kinds only) in-shared-memory weight decode
 //                 e4m3 -> bf16 or e2m1 x 2^(e-127) -> bf16
 //
 // Block scales ("[XPU] block-FP8 linear via torch scaled_mm": activations
@@ -39,7 +44,7 @@ enum { DT_BF16 = 1, DT_F32 = 2 };
 
 struct GemmMaps {
   CUtensorMap a;      // weights; fp8 box [128 B x 128 (64 for SiLU) rows], e2m1x2 box [64 B x rows]
-  CUtensorMap b[4];   // tokens; box rows 16 / 32 / 64 / 128
+  CUtensorMap b[5];   // tokens; box rows 16 / 32 / 64 / 128 / 256
 };
 
 struct GemmParams {
@@ -86,13 +91,19 @@ struct GemmParams {
 
 template <int KIND, int BT>
 struct Layout {
-  static constexpr int kThreads = (KIND == KIND_F8F8) ? 256 : 384;
+  static constexpr int EW = BT >= 128 ? 2 : 1;           // epilogue warpgroups
+  static constexpr int COLS = BT / EW;                     // token columns per epilogue WG
+  static constexpr int CONV_WARP0 = 4 + 4 * EW;
+  static constexpr int kThreads = 128 * (1 + EW + ((KIND == KIND_F8F8) ? 0 : 1));
   static constexpr int A_BYTES = (KIND == KIND_MXW) ? 128 * 64 : 128 * 128;
   static constexpr int B_BYTES = BT * 128 * ((KIND == KIND_F8F8) ? 1 : 2);
   static constexpr int C_BYTES = (KIND == KIND_F8F8) ? 0 : 128 * 256;
   static constexpr int CS = (KIND == KIND_F8F8) ? 0 : 2;
-  static constexpr int OUT_BYTES = 32 * 128 * 4;
-  static constexpr int MISC_BYTES = 2048;
+  static constexpr int STG = 16;                           // token columns staged per pass
+  static constexpr int LDC = (kThreads >= 512 || COLS > 64) ? 16 : 32;  // TMEM columns per load
+  static constexpr int OUT_BYTES = EW * STG * 128 * 4;
+  static constexpr int SSLOTS = 4;                         // scale ring depth
+  static constexpr int MISC_BYTES = 8192;
   static constexpr int BUDGET = 225 * 1024 - 1024;   // minus alignment slack
   static constexpr int FIXED = OUT_BYTES + MISC_BYTES + CS * C_BYTES;
   // F8F8: A and B stages in lock step; bf16 kinds: B ring 4 deep when it fits
@@ -107,6 +118,7 @@ struct Layout {
   static constexpr int TMEM_COLS = 2 * BT;
   static_assert(AS >= 2 && BS >= 2, "pipeline too shallow");
   static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory over budget");
+  static_assert(COLS % 32 == 0 && COLS <= 128, "epilogue column split");
 };
 
 struct Unit {
@@ -124,7 +136,7 @@ struct Unit {
 };
 
 __device__ __forceinline__ int box_variant(int n) {
-  return n <= 16 ? 0 : (n <= 32 ? 1 : (n <= 64 ? 2 : 3));
+  return n <= 16 ? 0 : (n <= 32 ? 1 : (n <= 64 ? 2 : (n <= 128 ? 3 : 4)));
 }
 
 template <int EPI, int BT>
@@ -238,7 +250,8 @@ template <int KIND, int EPI, int BT, bool PROMOTE>
 __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   using L = Layout<KIND, BT>;
-  constexpr int AS = L::AS, BS = L::BS, CS = L::CS;
+  constexpr int AS = L::AS, BS = L::BS, CS = L::CS, EW = L::EW, COLS = L::COLS;
+  constexpr int SSL = L::SSLOTS, STG = L::STG, LDC = L::LDC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -255,15 +268,20 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
   uint64_t* c_empty = c_full + 2;
   uint64_t* t_full = c_empty + 2;
   uint64_t* t_empty = t_full + 2;
-  uint64_t* drain = t_empty + 2;
-  uint64_t* epi_bar = drain + 1;     // bounded barrier of the 128 epilogue threads
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
+  uint64_t* s_full = t_empty + 2;
+  uint64_t* s_empty = s_full + SSL;
+  uint64_t* drain = s_empty + SSL;
+  uint64_t* epi_bar = drain + 1;     // bounded barriers, one per epilogue warpgroup
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 4);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  float* sAs = reinterpret_cast<float*>(misc + 1024);    // [2][BT] column scales
+  float* sAsc = reinterpret_cast<float*>(misc + 1024);            // [SSL][BT] column scales
+  float* sWr = reinterpret_cast<float*>(misc + 1024 + 4096);      // [SSL][128] row scales
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   WaitCtx wc{p.status, abort_flag, p.budget_ns};
+  // a row scale per TMEM lane is needed when Ws is not uniform over the tile
+  const bool lane_ws = PROMOTE && (p.block_n == 1 || EPI == EPI_SILU);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < AS; ++i) {
@@ -280,16 +298,18 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&t_full[i], 1);
-      mbar_init(&t_empty[i], 4);
+      mbar_init(&t_empty[i], 4 * EW);
+    }
+    for (int i = 0; i < SSL; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 4 * EW);
     }
     mbar_init(drain, 1);
-    mbar_init(epi_bar, 128);
+    for (int g = 0; g < EW; ++g) mbar_init(&epi_bar[g], 128);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&maps.a);
-  }
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&maps.a);
   if (warp == 1) {
     tmem_alloc(tmem_slot, L::TMEM_COLS);
     tmem_relinquish();
@@ -424,10 +444,68 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
         mbar_wait(drain, 0, dw);
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp == 3) {
+    // ---------------------------------------------------- scale loader
+    // Two slices of look-ahead in registers hide the global-load latency.
+    if (PROMOTE) {
+      constexpr int NA = BT / 32;
+      uint32_t is = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit U = get_unit<EPI, BT>(p, u);
+        float ra[2][NA], rw[2][4], ru[2];
+        auto fetch = [&](int kb, float* a, float* w, float& uni) {
+#pragma unroll
+          for (int i = 0; i < NA; ++i) {
+            const int j = lane + 32 * i;
+            a[i] = (p.a_scale != nullptr && j < U.rows)
+                       ? __ldg(p.a_scale + static_cast<int64_t>(U.m0 + j) * p.sa0 + kb * p.sa1)
+                       : 1.f;
+          }
+          if (lane_ws) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = lane + 32 * i;
+              const int row = lane_row_valid<EPI>(p, U, r) ? lane_row<EPI>(p, U, r) : 0;
+              w[i] = __ldg(p.w_scale + U.e * p.sw_e + (row / p.block_n) * p.sw0 + kb * p.sw1);
+            }
+            uni = 1.f;
+          } else {
+            uni = (p.block_n == 0)
+                      ? __ldg(p.w_scale)
+                      : __ldg(p.w_scale + U.e * p.sw_e + (U.n0 / p.block_n) * p.sw0 + kb * p.sw1);
+          }
+        };
+        auto publish = [&](const float* a, const float* w, float uni) -> bool {
+          const int slot = is % SSL;
+          if (!mbar_wait(&s_empty[slot], ((is / SSL) & 1) ^ 1, wc)) return false;
+#pragma unroll
+          for (int i = 0; i < NA; ++i) sAsc[slot * BT + lane + 32 * i] = a[i] * uni;
+          if (lane_ws) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sWr[slot * 128 + lane + 32 * i] = w[i];
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_full[slot]);
+          ++is;
+          return true;
+        };
+        fetch(U.kb0, ra[0], rw[0], ru[0]);
+        if (U.kb0 + 1 < U.kb1) fetch(U.kb0 + 1, ra[1], rw[1], ru[1]);
+        for (int kb = U.kb0; kb < U.kb1; kb += 2) {
+          if (!publish(ra[0], rw[0], ru[0])) goto scale_done;
+          if (kb + 2 < U.kb1) fetch(kb + 2, ra[0], rw[0], ru[0]);
+          if (kb + 1 < U.kb1) {
+            if (!publish(ra[1], rw[1], ru[1])) goto scale_done;
+            if (kb + 3 < U.kb1) fetch(kb + 3, ra[1], rw[1], ru[1]);
+          }
+        }
+      }
+    scale_done:;
+    }
+  } else if (warp >= L::CONV_WARP0) {
     // ------------------------------------------- weight decode to bf16
     if (KIND != KIND_F8F8) {
-      const int ct = threadIdx.x - 256;
+      const int ct = threadIdx.x - 32 * L::CONV_WARP0;
       uint32_t ia = 0, ic = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
@@ -477,17 +555,17 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
               uint32_t e = 127;
               if (col < p.mx_cols) e = __ldg(p.mx_scale + grow * p.mx_ld + col);
               // bf16 2^(e - 127 + 112) when representable; else two steps
-              __nv_bfloat162 sc;
+              __nv_bfloat162 sc2;
               uint32_t two_step = 0;
               {
                 const int ex = static_cast<int>(e) + 112;  // biased bf16 exponent of 2^(e-15)
                 if (ex >= 1 && ex <= 254) {
                   const uint32_t bits = (static_cast<uint32_t>(ex) << 7) * 0x10001u;
-                  sc = *reinterpret_cast<const __nv_bfloat162*>(&bits);
+                  sc2 = *reinterpret_cast<const __nv_bfloat162*>(&bits);
                 } else {
                   two_step = 1;
                   const uint32_t bits = 0x77807780u;
-                  sc = *reinterpret_cast<const __nv_bfloat162*>(&bits);
+                  sc2 = *reinterpret_cast<const __nv_bfloat162*>(&bits);
                 }
               }
               uint32_t w[16];
@@ -496,7 +574,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
               for (int j = 0; j < 4; ++j) {
 #pragma unroll
                 for (int bb = 0; bb < 4; ++bb)
-                  w[j * 4 + bb] = e2m1x2_to_bf16x2((in[j] >> (8 * bb)) & 0xFFu, sc);
+                  w[j * 4 + bb] = e2m1x2_to_bf16x2((in[j] >> (8 * bb)) & 0xFFu, sc2);
               }
               if (two_step) {
                 const float f = ldexpf(1.0f, static_cast<int>(e) - 127);
@@ -533,57 +611,56 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
     }
   } else if (warp >= 4) {
     // --------------------------------------------------------- epilogue
-    const int et = threadIdx.x - 128;                 // TMEM lane 0..127
+    const int g = (warp - 4) >> 2;                    // epilogue warpgroup
+    const int et = (threadIdx.x - 128) & 127;         // TMEM lane 0..127
+    const int col0 = g * COLS;                        // first token column of this WG
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t au = 0;
-    uint32_t eph = 0;   // phase of epi_bar
+    float* stg = sOut + g * (STG * 128);
+    uint32_t au = 0, is = 0, eph = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit U = get_unit<EPI, BT>(p, u);
-      const int nch = (U.rows + 31) >> 5;
-      const int wr = lane_row<EPI>(p, U, et);
-      const bool wr_ok = lane_row_valid<EPI>(p, U, et);
-      float acc[BT];
+      const int colv = max(0, min(COLS, U.rows - col0));   // valid columns of this WG
+      const int nld = (colv + LDC - 1) / LDC;
+      float acc[COLS];
       float fscale = 1.f;
       if (PROMOTE) {
 #pragma unroll
-        for (int j = 0; j < BT; ++j) acc[j] = 0.f;
-        const int64_t wrc = wr_ok ? wr : 0;
-        auto ws_at = [&](int kb) -> float {
-          if (p.block_n == 0) return __ldg(p.w_scale);
-          return __ldg(p.w_scale + U.e * p.sw_e + (wrc / p.block_n) * p.sw0 + kb * p.sw1);
-        };
-        auto as_at = [&](int kb) -> float {
-          if (p.a_scale == nullptr || et >= U.rows) return 1.f;
-          return __ldg(p.a_scale + static_cast<int64_t>(U.m0 + et) * p.sa0 + kb * p.sa1);
-        };
-        float as_nx = as_at(U.kb0);
-        float ws_nx = ws_at(U.kb0);
+        for (int j = 0; j < COLS; ++j) acc[j] = 0.f;
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
-          float* sa = sAs + (kb & 1) * BT;
-          if (et < BT) sa[et] = as_nx;
-          const float ws = ws_nx;
-          if (!group_sync(epi_bar, eph, wc)) goto epi_done;
-          if (kb + 1 < U.kb1) {
-            as_nx = as_at(kb + 1);
-            ws_nx = ws_at(kb + 1);
-          }
           const uint32_t buf = au & 1;
+          const int slot = is % SSL;
+          if (!mbar_wait(&s_full[slot], (is / SSL) & 1, wc)) goto epi_done;
           if (!mbar_wait(&t_full[buf], (au >> 1) & 1, wc)) goto epi_done;
           tc_fence_after();
+          const float* sc = sAsc + slot * BT + col0;
+          const float wr = lane_ws ? sWr[slot * 128 + et] : 1.f;
 #pragma unroll
-          for (int c = 0; c < BT / 32; ++c) {
-            if (c < nch) {
-              float v[32];
-              tmem_ld32(tmem_base + lane_addr + buf * BT + c * 32, v);
+          for (int c = 0; c < COLS / LDC; ++c) {
+            if (c < nld) {
+              float v[LDC];
+              tmem_ld<LDC>(tmem_base + lane_addr + buf * BT + col0 + c * LDC, v);
+              if (lane_ws) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                acc[c * 32 + j] = fmaf(v[j], ws * sa[c * 32 + j], acc[c * 32 + j]);
+                for (int j = 0; j < LDC; ++j) v[j] *= wr;
+              }
+#pragma unroll
+              for (int j = 0; j < LDC; j += 4) {
+                const float4 s4 = *reinterpret_cast<const float4*>(sc + c * LDC + j);
+                acc[c * LDC + j + 0] = fmaf(v[j + 0], s4.x, acc[c * LDC + j + 0]);
+                acc[c * LDC + j + 1] = fmaf(v[j + 1], s4.y, acc[c * LDC + j + 1]);
+                acc[c * LDC + j + 2] = fmaf(v[j + 2], s4.z, acc[c * LDC + j + 2]);
+                acc[c * LDC + j + 3] = fmaf(v[j + 3], s4.w, acc[c * LDC + j + 3]);
+              }
             }
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&t_empty[buf]);
+          if (lane == 0) {
+            mbar_arrive(&t_empty[buf]);
+            mbar_arrive(&s_empty[slot]);
+          }
           ++au;
+          ++is;
         }
       } else {
         if (p.block_n == 0 && p.w_scale != nullptr) fscale = __ldg(p.w_scale);
@@ -591,8 +668,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
         if (!mbar_wait(&t_full[buf], (au >> 1) & 1, wc)) goto epi_done;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < BT / 32; ++c) {
-          if (c < nch) tmem_ld32(tmem_base + lane_addr + buf * BT + c * 32, &acc[c * 32]);
+        for (int c = 0; c < COLS / LDC; ++c) {
+          if (c < nld) tmem_ld<LDC>(tmem_base + lane_addr + buf * BT + col0 + c * LDC, &acc[c * LDC]);
         }
         tc_fence_before();
         __syncwarp();
@@ -609,20 +686,26 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
             bias_u = load_bias(p, U.e * p.bias_e + p.n_half + U.n0 + l);
           }
         }
+        const int nl = (et & 31) * 4;          // DENSE / SCATTER: 4 weight rows per thread
+        const int n = U.n0 + nl;
+        float b4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (EPI != EPI_SILU && p.splits == 1) {
 #pragma unroll
-        for (int c = 0; c < BT / 32; ++c) {
-          if (c < nch) {
+          for (int i = 0; i < 4; ++i)
+            if (n + i < p.N) b4[i] = load_bias(p, U.e * p.bias_e + n + i);
+        }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sOut[j * 128 + et] = acc[c * 32 + j] * fscale;
-            if (!group_sync(epi_bar, eph, wc)) goto epi_done;
+        for (int c = 0; c < COLS / STG; ++c) {
+          if (c * STG < colv) {
+#pragma unroll
+            for (int j = 0; j < STG; ++j) stg[j * 128 + et] = acc[c * STG + j] * fscale;
+            if (!group_sync(&epi_bar[g], eph, wc)) goto epi_done;
             if (EPI == EPI_DENSE) {
-              const int nl = (et & 31) * 4;
-              const int n = U.n0 + nl;
-              for (int jj = et >> 5; jj < 32; jj += 4) {
-                const int col = c * 32 + jj;
+              for (int jj = et >> 5; jj < STG; jj += 4) {
+                const int col = col0 + c * STG + jj;
                 if (col >= U.rows) break;
                 const int m = U.m0 + col;
-                const float4 v = *reinterpret_cast<const float4*>(&sOut[jj * 128 + nl]);
+                const float4 v = *reinterpret_cast<const float4*>(&stg[jj * 128 + nl]);
                 float vv[4] = {v.x, v.y, v.z, v.w};
                 if (p.splits > 1) {
                   float* dstp = p.partial + (static_cast<int64_t>(U.split) * p.M + m) * p.N;
@@ -631,8 +714,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
                     if (n + i < p.N) dstp[n + i] = vv[i];
                 } else {
 #pragma unroll
-                  for (int i = 0; i < 4; ++i)
-                    if (n + i < p.N) vv[i] += load_bias(p, n + i);
+                  for (int i = 0; i < 4; ++i) vv[i] += b4[i];
                   const int64_t o = static_cast<int64_t>(m) * p.ldo + n;
                   if (p.out_dtype == DT_BF16) {
                     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
@@ -663,35 +745,33 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
             } else if (EPI == EPI_SILU) {
               const int l = et & 63;
               const bool ok = U.n0 + l < p.n_half;
-              for (int jj = et >> 6; jj < 32; jj += 2) {
-                const int col = c * 32 + jj;
+              for (int jj = et >> 6; jj < STG; jj += 2) {
+                const int col = col0 + c * STG + jj;
                 if (col >= U.rows) break;
                 if (ok) {
-                  const float g = sOut[jj * 128 + l] + bias_g;
-                  const float up = sOut[jj * 128 + 64 + l] + bias_u;
-                  const float a = g / (1.0f + expf(-g)) * up;
+                  const float gt = stg[jj * 128 + l] + bias_g;
+                  const float up = stg[jj * 128 + 64 + l] + bias_u;
+                  const float a = gt / (1.0f + expf(-gt)) * up;
                   reinterpret_cast<__nv_bfloat16*>(p.out)[static_cast<int64_t>(U.m0 + col) * p.ldo +
                                                           U.n0 + l] = __float2bfloat16_rn(a);
                 }
               }
             } else {  // EPI_SCATTER
-              const int nl = (et & 31) * 4;
-              const int n = U.n0 + nl;
-              for (int jj = et >> 5; jj < 32; jj += 4) {
-                const int col = c * 32 + jj;
+              for (int jj = et >> 5; jj < STG; jj += 4) {
+                const int col = col0 + c * STG + jj;
                 if (col >= U.rows) break;
                 const int slot =
                     __ldg(p.sorted_ids + static_cast<int64_t>(U.blk) * p.block_m + col);
                 const float rw = __ldg(p.route_w + slot);
-                const float4 v = *reinterpret_cast<const float4*>(&sOut[jj * 128 + nl]);
+                const float4 v = *reinterpret_cast<const float4*>(&stg[jj * 128 + nl]);
                 const float vv[4] = {v.x, v.y, v.z, v.w};
                 float* dst = reinterpret_cast<float*>(p.out) + static_cast<int64_t>(slot) * p.ldo;
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                  if (n + i < p.N) dst[n + i] = (vv[i] + load_bias(p, U.e * p.bias_e + n + i)) * rw;
+                  if (n + i < p.N) dst[n + i] = (vv[i] + b4[i]) * rw;
               }
             }
-            if (!group_sync(epi_bar, eph, wc)) goto epi_done;
+            if (!group_sync(&epi_bar[g], eph, wc)) goto epi_done;
           }
         }
       }

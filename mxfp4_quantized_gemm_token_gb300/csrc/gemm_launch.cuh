@@ -31,6 +31,11 @@ cudaError_t launch_gemm_bt(int bt, const GemmMaps& maps, const GemmParams& p, in
     case 32: return launch_gemm_inst<KIND, EPI, 32, PROMOTE>(maps, p, grid, stream);
     case 64: return launch_gemm_inst<KIND, EPI, 64, PROMOTE>(maps, p, grid, stream);
     case 128: return launch_gemm_inst<KIND, EPI, 128, PROMOTE>(maps, p, grid, stream);
+    case 256:
+      // 256 token columns: FP8 x FP8 only (the bf16 kinds do not fit shared memory)
+      if constexpr (KIND == KIND_F8F8)
+        return launch_gemm_inst<KIND, EPI, 256, PROMOTE>(maps, p, grid, stream);
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }

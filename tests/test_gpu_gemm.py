@@ -203,3 +203,18 @@ def test_full_size_block1x128_sampled_rows(oracle, M):
     rq, rs = oracle.per_token_group_quant_fp8(bits16(xf[ridx]), 128)
     _, rb = oracle.scaled_mm(rq, E4M3, rs, u8(wq), ws.cpu().numpy(), 1, 128)
     assert_bf16_close(flat[ridx], rb)
+
+
+@pytest.mark.parametrize("tile", [32, 64, 128, 256])
+def test_forced_token_tile_widths(oracle, tile):
+    """Every token-tile width (MMA N and epilogue split) on a ragged shape."""
+    try:
+        mxq.set_option(_lib.OPT_TILE_N, tile)
+        block_case(oracle, 300, 384, 640, 128, seed=41 + tile)
+        block_case(oracle, 70, 256, 384, 1, seed=43 + tile)
+        a, w, scale, bias = synth.per_tensor_fp8_problem(M=97, N=224, K=576, seed=44)
+        rf, rb = oracle.scaled_mm(bits16(a), BF16, None, u8(w), scale.numpy(), 0, 0, bias.numpy())
+        o = mxq.fp8_scaled_mm(a.cuda(), w.cuda(), scale.cuda(), None, bias=bias.cuda())
+        assert_bf16_close(o, rb)
+    finally:
+        mxq.set_option(_lib.OPT_TILE_N, 0)
