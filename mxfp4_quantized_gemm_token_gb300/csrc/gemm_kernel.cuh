@@ -91,7 +91,8 @@ struct GemmParams {
 
 template <int KIND, int BT>
 struct Layout {
-  static constexpr int EW = BT >= 128 ? 2 : 1;           // epilogue warpgroups
+  // epilogue warpgroups (one for up to 64 token columns, else two)
+  static constexpr int EW = BT >= 128 ? 2 : 1;
   static constexpr int COLS = BT / EW;                     // token columns per epilogue WG
   static constexpr int CONV_WARP0 = 4 + 4 * EW;
   static constexpr int kThreads = 128 * (1 + EW + ((KIND == KIND_F8F8) ? 0 : 1));
@@ -99,11 +100,12 @@ struct Layout {
   static constexpr int B_BYTES = BT * 128 * ((KIND == KIND_F8F8) ? 1 : 2);
   static constexpr int C_BYTES = (KIND == KIND_F8F8) ? 0 : 128 * 256;
   static constexpr int CS = (KIND == KIND_F8F8) ? 0 : 2;
-  static constexpr int STG = 16;                           // token columns staged per pass
-  static constexpr int LDC = (kThreads >= 512 || COLS > 64) ? 16 : 32;  // TMEM columns per load
+  static constexpr int STG = EW >= 4 ? 8 : 16;             // token columns staged per pass
+  // TMEM columns loaded per wait (bounded by registers: acc + one group live)
+  static constexpr int GRP = (kThreads >= 512 || COLS > 64) ? 32 : COLS;
   static constexpr int OUT_BYTES = EW * STG * 128 * 4;
-  static constexpr int SSLOTS = 4;                         // scale ring depth
-  static constexpr int MISC_BYTES = 8192;
+  static constexpr int SSLOTS = 8;                         // scale ring depth
+  static constexpr int MISC_BYTES = 16384;
   static constexpr int BUDGET = 225 * 1024 - 1024;   // minus alignment slack
   static constexpr int FIXED = OUT_BYTES + MISC_BYTES + CS * C_BYTES;
   // F8F8: A and B stages in lock step; bf16 kinds: B ring 4 deep when it fits
@@ -115,7 +117,8 @@ struct Layout {
   static constexpr int AS = AS_RAW > 12 ? 12 : AS_RAW;
   static constexpr int BS = (KIND == KIND_F8F8) ? AS : BS_PREF;
   static constexpr int TOTAL = AS * A_BYTES + CS * C_BYTES + BS * B_BYTES + OUT_BYTES + MISC_BYTES;
-  static constexpr int TMEM_COLS = 2 * BT;
+  static constexpr int NBUF = BT >= 256 ? 2 : 4;           // TMEM accumulator buffers
+  static constexpr int TMEM_COLS = NBUF * BT;
   static_assert(AS >= 2 && BS >= 2, "pipeline too shallow");
   static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory over budget");
   static_assert(COLS % 32 == 0 && COLS <= 128, "epilogue column split");
@@ -251,10 +254,11 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   using L = Layout<KIND, BT>;
   constexpr int AS = L::AS, BS = L::BS, CS = L::CS, EW = L::EW, COLS = L::COLS;
-  constexpr int SSL = L::SSLOTS, STG = L::STG, LDC = L::LDC;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int SSL = L::SSLOTS, STG = L::STG, GRP = L::GRP, NB = L::NBUF;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // align by offsetting the shared array itself (an integer round-trip would
+  // turn every shared access below into a generic one)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;
   uint8_t* sC = sA + AS * L::A_BYTES;
   uint8_t* sB = sC + CS * L::C_BYTES;
@@ -267,15 +271,15 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
   uint64_t* c_full = b_empty + 12;
   uint64_t* c_empty = c_full + 2;
   uint64_t* t_full = c_empty + 2;
-  uint64_t* t_empty = t_full + 2;
-  uint64_t* s_full = t_empty + 2;
+  uint64_t* t_empty = t_full + 4;
+  uint64_t* s_full = t_empty + 4;
   uint64_t* s_empty = s_full + SSL;
   uint64_t* drain = s_empty + SSL;
   uint64_t* epi_bar = drain + 1;     // bounded barriers, one per epilogue warpgroup
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 4);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* sAsc = reinterpret_cast<float*>(misc + 1024);            // [SSL][BT] column scales
-  float* sWr = reinterpret_cast<float*>(misc + 1024 + 4096);      // [SSL][128] row scales
+  float* sWr = reinterpret_cast<float*>(misc + 1024 + 8192);      // [SSL][128] row scales
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
       mbar_init(&c_full[i], 4);
       mbar_init(&c_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NB; ++i) {
       mbar_init(&t_full[i], 1);
       mbar_init(&t_empty[i], 4 * EW);
     }
@@ -393,9 +397,9 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
             (KIND == KIND_F8F8) ? idesc_e4m3(128, U.n_inst) : idesc_bf16(128, U.n_inst);
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
           const bool first = (kb == U.kb0), last = (kb == U.kb1 - 1);
-          const uint32_t buf = au & 1;
+          const uint32_t buf = au % NB;
           if (PROMOTE || first)
-            if (!mbar_wait(&t_empty[buf], ((au >> 1) & 1) ^ 1, wc)) goto mma_done;
+            if (!mbar_wait(&t_empty[buf], ((au / NB) & 1) ^ 1, wc)) goto mma_done;
           const int sa = (KIND == KIND_F8F8) ? ia % AS : ia % CS;
           if (KIND == KIND_F8F8) {
             if (!mbar_wait(&a_full[sa], (ia / AS) & 1, wc)) goto mma_done;
@@ -452,7 +456,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
       uint32_t is = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
-        float ra[2][NA], rw[2][4], ru[2];
+        float ra[4][NA], rw[4][4], ru[4];
         auto fetch = [&](int kb, float* a, float* w, float& uni) {
 #pragma unroll
           for (int i = 0; i < NA; ++i) {
@@ -489,14 +493,16 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
           ++is;
           return true;
         };
-        fetch(U.kb0, ra[0], rw[0], ru[0]);
-        if (U.kb0 + 1 < U.kb1) fetch(U.kb0 + 1, ra[1], rw[1], ru[1]);
-        for (int kb = U.kb0; kb < U.kb1; kb += 2) {
-          if (!publish(ra[0], rw[0], ru[0])) goto scale_done;
-          if (kb + 2 < U.kb1) fetch(kb + 2, ra[0], rw[0], ru[0]);
-          if (kb + 1 < U.kb1) {
-            if (!publish(ra[1], rw[1], ru[1])) goto scale_done;
-            if (kb + 3 < U.kb1) fetch(kb + 3, ra[1], rw[1], ru[1]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (U.kb0 + q < U.kb1) fetch(U.kb0 + q, ra[q], rw[q], ru[q]);
+        for (int kb = U.kb0; kb < U.kb1; kb += 4) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (kb + q < U.kb1) {
+              if (!publish(ra[q], rw[q], ru[q])) goto scale_done;
+              if (kb + q + 4 < U.kb1) fetch(kb + q + 4, ra[q], rw[q], ru[q]);
+            }
           }
         }
       }
@@ -620,56 +626,64 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit U = get_unit<EPI, BT>(p, u);
       const int colv = max(0, min(COLS, U.rows - col0));   // valid columns of this WG
-      const int nld = (colv + LDC - 1) / LDC;
+      const int ngr = (colv + GRP - 1) / GRP;              // column groups with valid tokens
       float acc[COLS];
       float fscale = 1.f;
       if (PROMOTE) {
 #pragma unroll
         for (int j = 0; j < COLS; ++j) acc[j] = 0.f;
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
-          const uint32_t buf = au & 1;
+          const uint32_t buf = au % NB;
           const int slot = is % SSL;
           if (!mbar_wait(&s_full[slot], (is / SSL) & 1, wc)) goto epi_done;
-          if (!mbar_wait(&t_full[buf], (au >> 1) & 1, wc)) goto epi_done;
+          if (!mbar_wait(&t_full[buf], (au / NB) & 1, wc)) goto epi_done;
           tc_fence_after();
           const float* sc = sAsc + slot * BT + col0;
           const float wr = lane_ws ? sWr[slot * 128 + et] : 1.f;
 #pragma unroll
-          for (int c = 0; c < COLS / LDC; ++c) {
-            if (c < nld) {
-              float v[LDC];
-              tmem_ld<LDC>(tmem_base + lane_addr + buf * BT + col0 + c * LDC, v);
+          for (int c = 0; c < COLS / GRP; ++c) {
+            if (c < ngr) {
+              float v[GRP];
+              tmem_ld<GRP>(tmem_base + lane_addr + buf * BT + col0 + c * GRP, v);
+              if (c == COLS / GRP - 1 || c + 1 == ngr) {
+                // the last TMEM read of this slice is done: hand the buffer
+                // back to the MMA before doing the arithmetic
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&t_empty[buf]);
+              }
               if (lane_ws) {
 #pragma unroll
-                for (int j = 0; j < LDC; ++j) v[j] *= wr;
+                for (int j = 0; j < GRP; ++j) v[j] *= wr;
               }
 #pragma unroll
-              for (int j = 0; j < LDC; j += 4) {
-                const float4 s4 = *reinterpret_cast<const float4*>(sc + c * LDC + j);
-                acc[c * LDC + j + 0] = fmaf(v[j + 0], s4.x, acc[c * LDC + j + 0]);
-                acc[c * LDC + j + 1] = fmaf(v[j + 1], s4.y, acc[c * LDC + j + 1]);
-                acc[c * LDC + j + 2] = fmaf(v[j + 2], s4.z, acc[c * LDC + j + 2]);
-                acc[c * LDC + j + 3] = fmaf(v[j + 3], s4.w, acc[c * LDC + j + 3]);
+              for (int j = 0; j < GRP; j += 4) {
+                const float4 s4 = *reinterpret_cast<const float4*>(sc + c * GRP + j);
+                acc[c * GRP + j + 0] = fmaf(v[j + 0], s4.x, acc[c * GRP + j + 0]);
+                acc[c * GRP + j + 1] = fmaf(v[j + 1], s4.y, acc[c * GRP + j + 1]);
+                acc[c * GRP + j + 2] = fmaf(v[j + 2], s4.z, acc[c * GRP + j + 2]);
+                acc[c * GRP + j + 3] = fmaf(v[j + 3], s4.w, acc[c * GRP + j + 3]);
               }
             }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&t_empty[buf]);
-            mbar_arrive(&s_empty[slot]);
+          if (ngr == 0) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&t_empty[buf]);
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[slot]);
           ++au;
           ++is;
         }
       } else {
         if (p.block_n == 0 && p.w_scale != nullptr) fscale = __ldg(p.w_scale);
-        const uint32_t buf = au & 1;
-        if (!mbar_wait(&t_full[buf], (au >> 1) & 1, wc)) goto epi_done;
+        const uint32_t buf = au % NB;
+        if (!mbar_wait(&t_full[buf], (au / NB) & 1, wc)) goto epi_done;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < COLS / LDC; ++c) {
-          if (c < nld) tmem_ld<LDC>(tmem_base + lane_addr + buf * BT + col0 + c * LDC, &acc[c * LDC]);
+        for (int c = 0; c < COLS / GRP; ++c) {
+          if (c < ngr) tmem_ld<GRP>(tmem_base + lane_addr + buf * BT + col0 + c * GRP, &acc[c * GRP]);
         }
         tc_fence_before();
         __syncwarp();
