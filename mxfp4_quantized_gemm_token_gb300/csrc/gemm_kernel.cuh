@@ -366,7 +366,10 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
         const CUtensorMap* mb = &maps.b[U.bvar];
         for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
           const int s = it % BS;
-          if (!mbar_wait(&b_empty[s], ((it / BS) & 1) ^ 1, wc)) goto prod_b_done;
+          // FP8 x FP8: A and B stages advance together and are released by
+          // one commit (a_empty); the bf16 kinds release B on its own ring
+          uint64_t* rel = (KIND == KIND_F8F8) ? &a_empty[s] : &b_empty[s];
+          if (!mbar_wait(rel, ((it / BS) & 1) ^ 1, wc)) goto prod_b_done;
           uint8_t* dst = sB + s * L::B_BYTES;
           if (KIND == KIND_F8F8) {
             mbar_expect_tx(&b_full[s], brows * 128);
@@ -431,7 +434,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
             }
             mma_commit(&c_empty[sa]);
           }
-          mma_commit(&b_empty[sb]);
+          if (KIND != KIND_F8F8) mma_commit(&b_empty[sb]);
           ++ia;
           ++ib;
           if (PROMOTE || last) {
@@ -653,16 +656,27 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
                 if (lane == 0) mbar_arrive(&t_empty[buf]);
               }
               if (lane_ws) {
+                const float2 w2 = make_float2(wr, wr);
 #pragma unroll
-                for (int j = 0; j < GRP; ++j) v[j] *= wr;
+                for (int j = 0; j < GRP; j += 2) {
+                  const float2 p2 = __fmul2_rn(make_float2(v[j], v[j + 1]), w2);
+                  v[j] = p2.x;
+                  v[j + 1] = p2.y;
+                }
               }
+              // packed fp32 FMA: two accumulator elements per instruction
 #pragma unroll
               for (int j = 0; j < GRP; j += 4) {
                 const float4 s4 = *reinterpret_cast<const float4*>(sc + c * GRP + j);
-                acc[c * GRP + j + 0] = fmaf(v[j + 0], s4.x, acc[c * GRP + j + 0]);
-                acc[c * GRP + j + 1] = fmaf(v[j + 1], s4.y, acc[c * GRP + j + 1]);
-                acc[c * GRP + j + 2] = fmaf(v[j + 2], s4.z, acc[c * GRP + j + 2]);
-                acc[c * GRP + j + 3] = fmaf(v[j + 3], s4.w, acc[c * GRP + j + 3]);
+                float* a = acc + c * GRP + j;
+                const float2 lo = __ffma2_rn(make_float2(v[j], v[j + 1]), make_float2(s4.x, s4.y),
+                                             make_float2(a[0], a[1]));
+                const float2 hi = __ffma2_rn(make_float2(v[j + 2], v[j + 3]), make_float2(s4.z, s4.w),
+                                             make_float2(a[2], a[3]));
+                a[0] = lo.x;
+                a[1] = lo.y;
+                a[2] = hi.x;
+                a[3] = hi.y;
               }
             }
           }
