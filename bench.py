@@ -332,6 +332,108 @@ def run_profile(args, local):
     return 0
 
 
+# ---------------------------------------------------------- other workloads
+
+def _timed_calls(fn, reps, flush):
+    """Median device time (ms) of fn() over reps calls, L2 flushed before each."""
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def run_workloads(args, local):
+    """One JSON line per shape of the other hot-path configurations (for the
+    results tables): per-tensor W8A16, [1,128] block W8A8, fused MoE FP8-block
+    and MXFP4.  Each call is timed alone with L2 flushed (512 MB write) before it."""
+    import mxfp4_quantized_gemm_token_gb300 as mxq
+    from mxfp4_quantized_gemm_token_gb300 import synth
+    dev = torch.device("cuda", local)
+    pk, _ = peaks()
+    hbm = pk["hbm_gbs"]
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    reps = args.steps
+    names = args.workload.split(",")
+    out = []
+
+    def emit(d):
+        d["workload"] = name
+        print(json.dumps(d), flush=True)
+
+    for name in names:
+        if name == "pertensor":
+            a, w, scale, bias = synth.per_tensor_fp8_problem(seed=0)
+            a, w, scale, bias = a.to(dev), w.to(dev), scale.to(dev), bias.to(dev)
+            for _ in range(args.warmup):
+                mxq.fp8_per_tensor_linear(a, w, scale, bias)
+            ms = _timed_calls(lambda: mxq.fp8_per_tensor_linear(a, w, scale, bias), reps, flush)
+            byts = 97 * 576 * 2 + 224 * 576 + 224 * 4 + 97 * 224 * 2
+            emit({"M": 97, "N": 224, "K": 576, "us": ms * 1e3,
+                  "TFLOPs": 2 * 97 * 224 * 576 / ms / 1e9, "GBs": byts / ms / 1e6})
+        elif name == "block1x128":
+            w, ws = synth.block_fp8_weight(4096, 7168, 1, seed=1, device=dev)
+            for M in (1, 64, 2048):
+                if M >= 64:
+                    base = synth.activations(M, 7168 + 128, seed=M, device=dev).view(2, M // 2, 7296)
+                    x = base[:, :, :7168]
+                else:
+                    x = synth.activations(M, 7168, seed=M, device=dev)
+                f = lambda: mxq.w8a8_block_fp8_linear(x, w, [1, 128], ws)
+                for _ in range(args.warmup):
+                    f()
+                ms = _timed_calls(f, reps, flush)
+                byts = 4096 * 7168 + 4096 * 56 * 4 + M * 7168 * 2 + M * 4096 * 2
+                emit({"M": M, "N": 4096, "K": 7168, "us": ms * 1e3,
+                      "TFLOPs": 2 * M * 4096 * 7168 / ms / 1e9, "GBs": byts / ms / 1e6,
+                      "hbm_frac": byts / ms / 1e6 / hbm})
+        elif name in ("moe_fp8", "moe_mxfp4"):
+            fp8 = name == "moe_fp8"
+            E, topk, K, N = (256, 8, 7168, 2048) if fp8 else (128, 4, 2880, 2880)
+            Ts = (4, 32, 256, 1024) if fp8 else (1, 32, 64, 512)
+            if fp8:
+                w1, s1, w2, s2 = synth.moe_fp8_weights(E, N, K, seed=0, device=dev)
+                b1 = b2 = None
+                per_expert = 2 * N * K + K * N + (s1[0].numel() + s2[0].numel()) * 4
+                wt = mxq.W_FP8_BLOCK128
+            else:
+                w1, s1, w2, s2 = synth.moe_mxfp4_weights(E, N, K, seed=0, device=dev)
+                b1, b2 = synth.moe_biases(E, N, K, seed=1, device=dev)
+                per_expert = (2 * N * K + K * N) // 2 + (2 * N * K + K * N) // 32 + (2 * N + K) * 4
+                wt = mxq.W_MXFP4
+            for T in Ts:
+                for routing in ("uniform", "zipf"):
+                    rf = synth.routing_uniform if routing == "uniform" else synth.routing_zipf
+                    tw, ids = rf(T, E, topk, seed=T)
+                    touched = synth.distinct_experts(ids)
+                    x = synth.activations(T, K, seed=T, scale_div=10, device=dev)
+                    tw, ids = tw.to(dev), ids.to(dev)
+                    bm = args.block_m
+                    ws = torch.empty(1, dtype=torch.uint8, device=dev)
+                    import ctypes
+                    sz = ctypes.c_size_t(0)
+                    mxq.check(mxq._lib.load().mxq_fused_experts_workspace_size(
+                        T, K, E, N, topk, bm, wt, ctypes.byref(sz)))
+                    ws = torch.empty(sz.value, dtype=torch.uint8, device=dev)
+                    f = lambda: mxq.fused_experts(x, w1, s1, w2, s2, tw, ids, wtype=wt, w1_bias=b1,
+                                                  w2_bias=b2, block_m=bm, workspace=ws)
+                    for _ in range(args.warmup):
+                        f()
+                    mxq.sync_status(dev)
+                    ms = _timed_calls(f, reps, flush)
+                    byts = touched * per_expert + T * K * 4
+                    flops = T * topk * (2 * K * 2 * N + 2 * N * K)
+                    emit({"T": T, "routing": routing, "experts_touched": touched, "block_m": bm,
+                          "us": ms * 1e3, "TFLOPs": flops / ms / 1e9, "GBs": byts / ms / 1e6,
+                          "hbm_frac": byts / ms / 1e6 / hbm})
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -339,6 +441,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mxq", choices=["mxq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="",
+                    help="comma list of pertensor, block1x128, moe_fp8, moe_mxfp4 (tables only)")
+    ap.add_argument("--block-m", type=int, default=64)
     ap.add_argument("--profile", type=int, default=0,
                     help="run 3 launches of quant + GEMM at this M only (for ncu)")
     ap.add_argument("--traffic", type=float, default=None,
@@ -351,6 +456,8 @@ def main():
         return run_reference(args, world, rank)
     if args.profile:
         return run_profile(args, local)
+    if args.workload:
+        return run_workloads(args, local)
     return run_gpu(args, world, rank, local)
 
 
