@@ -204,18 +204,23 @@ namespace {
 struct MmPlan {
   int bt, kind, tiles_n, tiles_m, nkb, splits, kb_per_split;
   bool promote;
+  bool normal;   // tokens on the MMA M side (EPI_NORMAL)
 };
 
 MmPlan plan_mm(int64_t M, int64_t N, int64_t K, int32_t a_dtype, bool block, bool has_ascale,
-               int num_sms) {
+               int num_sms, bool uniform_wscale = true) {
   MmPlan pl;
   pl.kind = a_dtype == MXQ_E4M3 ? KIND_F8F8 : KIND_F8W;
   pl.bt = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
   const int64_t tile = option(MXQ_OPT_TILE_N);
   if (tile > 0) pl.bt = (tile == 256 && pl.kind != KIND_F8F8) ? 128 : static_cast<int>(tile);
+  // Large M with a weight scale that is uniform over 128 weight rows: put the
+  // tokens on the MMA M side so each TMEM lane's slice scale is one scalar.
+  pl.normal = pl.kind == KIND_F8F8 && has_ascale && uniform_wscale && M > 128 && tile == 0;
+  if (pl.normal) pl.bt = 128;
   pl.promote = block || has_ascale;
-  pl.tiles_n = static_cast<int>(cdiv(N, 128));
-  pl.tiles_m = static_cast<int>(cdiv(M, pl.bt));
+  pl.tiles_n = static_cast<int>(cdiv(N, pl.normal ? pl.bt : 128));
+  pl.tiles_m = static_cast<int>(cdiv(M, pl.normal ? 128 : pl.bt));
   pl.nkb = static_cast<int>(cdiv(K, 128));
   const int64_t units = static_cast<int64_t>(pl.tiles_n) * pl.tiles_m;
   int splits = static_cast<int>(option(MXQ_OPT_SPLIT_K));
@@ -297,7 +302,7 @@ extern "C" mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t 
   std::string err;
   if (!device_info(&d, &err)) return fail(MXQ_ERR_UNSUPPORTED, err);
   const int sms = sms_for_grid(d);
-  MmPlan pl = plan_mm(M, N, K, a_dtype, block, a_scale != nullptr, sms);
+  MmPlan pl = plan_mm(M, N, K, a_dtype, block, a_scale != nullptr, sms, block_n != 1);
   if (pl.splits > 1 &&
       (workspace == nullptr || ws_bytes < static_cast<size_t>(pl.splits) * M * N * sizeof(float) ||
        (reinterpret_cast<uintptr_t>(workspace) & 15) != 0)) {
@@ -307,11 +312,20 @@ extern "C" mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t 
 
   GemmMaps maps;
   std::memset(&maps, 0, sizeof(maps));
-  if (!make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, K, N, ldw, 128, 128,
-                   CU_TENSOR_MAP_SWIZZLE_128B, &err))
-    return fail(MXQ_ERR_CUDA, err);
   const int bv = pl.bt == 32 ? 1 : (pl.bt == 64 ? 2 : (pl.bt == 128 ? 3 : 4));
-  if (a_dtype == MXQ_E4M3) {
+  if (pl.normal) {
+    // MMA A = tokens (128-row boxes), MMA B = weights (bt-row boxes)
+    if (!make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, lda, 128, 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B, &err) ||
+        !make_map_2d(&maps.b[bv], CU_TENSOR_MAP_DATA_TYPE_UINT8, W, K, N, ldw, 128, pl.bt,
+                     CU_TENSOR_MAP_SWIZZLE_128B, &err))
+      return fail(MXQ_ERR_CUDA, err);
+  } else if (!make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, K, N, ldw, 128, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B, &err)) {
+    return fail(MXQ_ERR_CUDA, err);
+  }
+  if (pl.normal) {
+  } else if (a_dtype == MXQ_E4M3) {
     if (!make_map_2d(&maps.b[bv], CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, lda, 128, pl.bt,
                      CU_TENSOR_MAP_SWIZZLE_128B, &err))
       return fail(MXQ_ERR_CUDA, err);
@@ -348,12 +362,17 @@ extern "C" mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t 
   p.budget_ns = static_cast<unsigned long long>(option(MXQ_OPT_WAIT_BUDGET_NS));
   p.inject_stall = static_cast<int>(option(MXQ_OPT_INJECT_STALL));
   const uintptr_t ob = reinterpret_cast<uintptr_t>(out);
-  p.vec_ok = (ldo % 4 == 0) && ((out_dtype == MXQ_BF16) ? (ob & 7) == 0 : (ob & 15) == 0);
+  if (pl.normal)   // 16-byte row chunks of 8 outputs
+    p.vec_ok = (out_dtype == MXQ_BF16) ? (ldo % 8 == 0 && (ob & 15) == 0)
+                                        : (ldo % 4 == 0 && (ob & 15) == 0);
+  else
+    p.vec_ok = (ldo % 4 == 0) && ((out_dtype == MXQ_BF16) ? (ob & 7) == 0 : (ob & 15) == 0);
 
   const int64_t units = static_cast<int64_t>(pl.tiles_n) * pl.tiles_m * pl.splits;
   const int grid = static_cast<int>(std::min<int64_t>(units, sms));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_gemm(pl.kind, EPI_DENSE, pl.bt, pl.promote, maps, p, grid, st);
+  cudaError_t e = launch_gemm(pl.kind, pl.normal ? EPI_NORMAL : EPI_DENSE, pl.bt, pl.promote,
+                              maps, p, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "scaled-mm launch");
   if (pl.splits > 1) {
     e = launch_splitk_reduce(p.partial, pl.splits, M, N, bias, p.bias_dtype, out, out_dtype, ldo,

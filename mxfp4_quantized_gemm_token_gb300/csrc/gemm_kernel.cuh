@@ -39,7 +39,11 @@
 namespace mxq {
 
 enum { KIND_F8F8 = 0, KIND_F8W = 1, KIND_MXW = 2 };
-enum { EPI_DENSE = 0, EPI_SILU = 1, EPI_SCATTER = 2 };
+// EPI_DENSE: weights on the MMA M side (swap-AB; decode and [1,128] blocks)
+// EPI_NORMAL: tokens on the MMA M side, weights on N (large M with uniform
+//             [128,128] / per-tensor weight scales: the slice scale is one
+//             scalar per TMEM lane, As(m, kb) * Ws(kb))
+enum { EPI_DENSE = 0, EPI_SILU = 1, EPI_SCATTER = 2, EPI_NORMAL = 3 };
 enum { DT_BF16 = 1, DT_F32 = 2 };
 
 struct GemmMaps {
@@ -133,7 +137,8 @@ struct Unit {
   int blk;      // expert block (grouped)
   int split;
   int tn;
-  int wrow0, wrow1;   // TMA row coordinates of the weight box(es)
+  int wrow0, wrow1;   // TMA row coordinates of the MMA-A box(es)
+  int brow;           // TMA row coordinate of the MMA-B box
   int n_inst;   // MMA instruction N
   int bvar;     // token box variant (rows 16 << bvar)
 };
@@ -151,17 +156,28 @@ __device__ __forceinline__ Unit get_unit(const GemmParams& p, int u) {
     const int r = u - U.tn * per;
     const int tm = r / p.splits;
     U.split = r - tm * p.splits;
-    U.n0 = U.tn * 128;
-    U.m0 = tm * BT;
-    U.rows = min(BT, p.M - U.m0);
     U.kb0 = U.split * p.kb_per_split;
     U.kb1 = min(p.nkb, U.kb0 + p.kb_per_split);
     U.e = 0;
     U.blk = 0;
-    U.wrow0 = U.n0;
-    U.wrow1 = U.n0;
     U.n_inst = BT;
     U.bvar = box_variant(BT);
+    if (EPI == EPI_NORMAL) {
+      // 128 tokens (A, TMEM lanes) x BT weight rows (B, TMEM columns)
+      U.n0 = U.tn * BT;
+      U.m0 = tm * 128;
+      U.rows = min(128, p.M - U.m0);
+      U.wrow0 = U.m0;
+      U.wrow1 = U.m0;
+      U.brow = U.n0;
+    } else {
+      U.n0 = U.tn * 128;
+      U.m0 = tm * BT;
+      U.rows = min(BT, p.M - U.m0);
+      U.wrow0 = U.n0;
+      U.wrow1 = U.n0;
+      U.brow = U.m0;
+    }
   } else {
     U.blk = u / p.tiles_n;
     U.tn = u - U.blk * p.tiles_n;
@@ -186,6 +202,7 @@ __device__ __forceinline__ Unit get_unit(const GemmParams& p, int u) {
     const int fit = ((U.rows + 15) / 16) * 16;
     U.n_inst = (U.rows <= p.narrow_max) ? min(fit, BT) : BT;
     U.bvar = box_variant(U.n_inst);
+    U.brow = U.m0;
   }
   return U;
 }
@@ -373,11 +390,11 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
           uint8_t* dst = sB + s * L::B_BYTES;
           if (KIND == KIND_F8F8) {
             mbar_expect_tx(&b_full[s], brows * 128);
-            tma_load_2d(dst, mb, &b_full[s], kb * 128, U.m0);
+            tma_load_2d(dst, mb, &b_full[s], kb * 128, U.brow);
           } else {
             mbar_expect_tx(&b_full[s], brows * 256);
-            tma_load_2d(dst, mb, &b_full[s], kb * 128, U.m0);
-            tma_load_2d(dst + brows * 128, mb, &b_full[s], kb * 128 + 64, U.m0);
+            tma_load_2d(dst, mb, &b_full[s], kb * 128, U.brow);
+            tma_load_2d(dst + brows * 128, mb, &b_full[s], kb * 128 + 64, U.brow);
           }
         }
       }
@@ -454,7 +471,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
   } else if (warp == 3) {
     // ---------------------------------------------------- scale loader
     // Two slices of look-ahead in registers hide the global-load latency.
-    if (PROMOTE) {
+    if (PROMOTE && EPI != EPI_NORMAL) {
       constexpr int NA = BT / 32;
       uint32_t is = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
@@ -618,6 +635,120 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
       }
     conv_done:;
     }
+  } else if (warp >= 4 && EPI == EPI_NORMAL) {
+    // ------------------------------------- epilogue, tokens on TMEM lanes
+    // Thread = token row m; its slice scale As(m, kb) * Ws(blk, kb) is one
+    // scalar, so promotion is one packed FMA per pair of accumulators.
+    const int g = (warp - 4) >> 2;
+    const int et = (threadIdx.x - 128) & 127;
+    const int col0 = g * COLS;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t au = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const Unit U = get_unit<EPI, BT>(p, u);
+      const bool mrow = et < U.rows;
+      const int m = U.m0 + (mrow ? et : 0);
+      const int ncv = min(BT, p.N - U.n0);              // valid weight columns of the tile
+      const int colv = max(0, min(COLS, ncv - col0));
+      const int ngr = (colv + GRP - 1) / GRP;
+      const int64_t wblk = (U.n0 + col0) / 128;
+      const float* arow = p.a_scale + static_cast<int64_t>(m) * p.sa0;
+      auto scale_at = [&](int kb) -> float {
+        const float w = (p.block_n == 0) ? __ldg(p.w_scale) : __ldg(p.w_scale + wblk * p.sw0 + kb * p.sw1);
+        return __ldg(arow + kb * p.sa1) * w;
+      };
+      float acc[COLS];
+#pragma unroll
+      for (int j = 0; j < COLS; ++j) acc[j] = 0.f;
+      float sc_nx = scale_at(U.kb0);
+      for (int kb = U.kb0; kb < U.kb1; ++kb) {
+        const float sc = sc_nx;
+        if (kb + 1 < U.kb1) sc_nx = scale_at(kb + 1);
+        const uint32_t buf = au % NB;
+        if (!mbar_wait(&t_full[buf], (au / NB) & 1, wc)) goto epin_done;
+        tc_fence_after();
+        const float2 s2 = make_float2(sc, sc);
+#pragma unroll
+        for (int c = 0; c < COLS / GRP; ++c) {
+          if (c < ngr) {
+            float v[GRP];
+            tmem_ld<GRP>(tmem_base + lane_addr + buf * BT + col0 + c * GRP, v);
+            if (c == COLS / GRP - 1 || c + 1 == ngr) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&t_empty[buf]);
+            }
+#pragma unroll
+            for (int j = 0; j < GRP; j += 2) {
+              const float2 r = __ffma2_rn(make_float2(v[j], v[j + 1]), s2,
+                                          make_float2(acc[c * GRP + j], acc[c * GRP + j + 1]));
+              acc[c * GRP + j] = r.x;
+              acc[c * GRP + j + 1] = r.y;
+            }
+          }
+        }
+        if (ngr == 0) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&t_empty[buf]);
+        }
+        ++au;
+      }
+      // ------------------------------------------------------- output
+      if (mrow && colv > 0) {
+        const int nbase = U.n0 + col0;
+#pragma unroll
+        for (int c8 = 0; c8 < COLS / 8; ++c8) {
+          const int n = nbase + c8 * 8;
+          if (c8 * 8 >= colv) break;
+          float vv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) vv[i] = acc[c8 * 8 + i];
+          const bool full8 = (n + 8 <= p.N);
+          if (p.splits > 1) {
+            float* dstp = p.partial + (static_cast<int64_t>(U.split) * p.M + U.m0 + et) * p.N + n;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (n + i < p.N) dstp[i] = vv[i];
+            continue;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (n + i < p.N) vv[i] += load_bias(p, n + i);
+          const int64_t o = static_cast<int64_t>(U.m0 + et) * p.ldo + n;
+          if (p.out_dtype == DT_BF16) {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
+            if (p.vec_ok && full8) {
+              uint4 pk;
+              __nv_bfloat162 t0 = __floats2bfloat162_rn(vv[0], vv[1]);
+              __nv_bfloat162 t1 = __floats2bfloat162_rn(vv[2], vv[3]);
+              __nv_bfloat162 t2 = __floats2bfloat162_rn(vv[4], vv[5]);
+              __nv_bfloat162 t3 = __floats2bfloat162_rn(vv[6], vv[7]);
+              pk.x = *reinterpret_cast<uint32_t*>(&t0);
+              pk.y = *reinterpret_cast<uint32_t*>(&t1);
+              pk.z = *reinterpret_cast<uint32_t*>(&t2);
+              pk.w = *reinterpret_cast<uint32_t*>(&t3);
+              *reinterpret_cast<uint4*>(dst) = pk;
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (n + i < p.N) dst[i] = __float2bfloat16_rn(vv[i]);
+            }
+          } else {
+            float* dst = reinterpret_cast<float*>(p.out) + o;
+            if (p.vec_ok && full8) {
+              reinterpret_cast<float4*>(dst)[0] = make_float4(vv[0], vv[1], vv[2], vv[3]);
+              reinterpret_cast<float4*>(dst)[1] = make_float4(vv[4], vv[5], vv[6], vv[7]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (n + i < p.N) dst[i] = vv[i];
+            }
+          }
+        }
+      }
+    }
+  epin_done:;
   } else if (warp >= 4) {
     // --------------------------------------------------------- epilogue
     const int g = (warp - 4) >> 2;                    // epilogue warpgroup
