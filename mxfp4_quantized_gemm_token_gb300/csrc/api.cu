@@ -217,7 +217,7 @@ MmPlan plan_mm(int64_t M, int64_t N, int64_t K, int32_t a_dtype, bool block, boo
   // Large M with a weight scale that is uniform over 128 weight rows: put the
   // tokens on the MMA M side so each TMEM lane's slice scale is one scalar.
   pl.normal = pl.kind == KIND_F8F8 && has_ascale && uniform_wscale && M > 128 && tile == 0;
-  if (pl.normal) pl.bt = 128;
+  if (pl.normal) pl.bt = (M >= 512 && N >= 4096) ? 256 : 128;
   pl.promote = block || has_ascale;
   pl.tiles_n = static_cast<int>(cdiv(N, pl.normal ? pl.bt : 128));
   pl.tiles_m = static_cast<int>(cdiv(M, pl.normal ? 128 : pl.bt));

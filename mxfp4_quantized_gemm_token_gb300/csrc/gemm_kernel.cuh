@@ -96,7 +96,7 @@ struct GemmParams {
 template <int KIND, int BT>
 struct Layout {
   // epilogue warpgroups (one for up to 64 token columns, else two)
-  static constexpr int EW = BT >= 128 ? 2 : 1;
+  static constexpr int EW = (KIND == KIND_F8F8 && BT >= 256) ? 4 : (BT >= 128 ? 2 : 1);
   static constexpr int COLS = BT / EW;                     // token columns per epilogue WG
   static constexpr int CONV_WARP0 = 4 + 4 * EW;
   static constexpr int kThreads = 128 * (1 + EW + ((KIND == KIND_F8F8) ? 0 : 1));
@@ -106,7 +106,7 @@ struct Layout {
   static constexpr int CS = (KIND == KIND_F8F8) ? 0 : 2;
   static constexpr int STG = EW >= 4 ? 8 : 16;             // token columns staged per pass
   // TMEM columns loaded per wait (bounded by registers: acc + one group live)
-  static constexpr int GRP = (kThreads >= 512 || COLS > 64) ? 32 : COLS;
+  static constexpr int GRP = kThreads >= 640 ? 16 : ((kThreads >= 512 || COLS > 64) ? 32 : COLS);
   static constexpr int OUT_BYTES = EW * STG * 128 * 4;
   static constexpr int SSLOTS = 8;                         // scale ring depth
   static constexpr int MISC_BYTES = 16384;
