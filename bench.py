@@ -32,6 +32,12 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 N_W, K_W = 18432, 7168
+# DRAM bytes (read + write) of one launch of the dominant kernel, from
+# `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
+#  -k regex:gemm_kernel -s 1 -c 1 python bench.py --profile 4096`
+# (summarised in profiles/); set to None whenever that kernel changes.
+DOMINANT_KERNEL = "gemm_kernel<F8F8, NORMAL, 256, promote> (M=4096)"
+DOMINANT_TRAFFIC_BYTES = 168.44e6 + 127.77e6
 M_SET = (1, 8, 17, 128, 1024, 4096)
 METRIC = "FP8 block-scaled W8A8 linear (quant + scaled GEMM) throughput, [128,128] weights"
 WORKLOAD = ("block-FP8 W8A8 linear, W e4m3 [18432, 7168] with [128,128] fp32 block scales, "
@@ -63,7 +69,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -161,7 +167,7 @@ def flops_block128():
 _ORACLE_INPUTS = []
 
 
-def cpu_oracle_sample(seconds: float = 12.0, max_rows: int = 64):
+def cpu_oracle_sample(seconds: float = 12.0, max_rows: int = 512):
     """The oracle (plain C, fp64) on a bounded sample of the default workload:
     whole rows of the M = 4096 GEMM (activation quantization + all 18432
     outputs of each row), rows added until the time budget is spent."""
@@ -170,7 +176,7 @@ def cpu_oracle_sample(seconds: float = 12.0, max_rows: int = 64):
     if not _ORACLE_INPUTS:
         from mxfp4_quantized_gemm_token_gb300 import synth
         wq, ws = synth.block_fp8_weight(N_W, K_W, 128, seed=0)
-        x = synth.activations(64, K_W, seed=1000 + 4096)
+        x = synth.activations(512, K_W, seed=1000 + 4096)
         _ORACLE_INPUTS.extend([wq.view(torch.uint8).numpy(), ws.numpy(),
                                x.view(torch.int16).numpy().view(np.uint16)])
     w_np, ws_np, xb = _ORACLE_INPUTS
@@ -197,7 +203,7 @@ def run_reference(args, world, rank):
     t0 = time.perf_counter()
     res = None
     for _ in range(args.steps):
-        res = cpu_oracle_sample(seconds=max(3.0, 20.0 / max(1, args.steps)), max_rows=64)
+        res = cpu_oracle_sample(seconds=max(3.0, 20.0 / max(1, args.steps)), max_rows=512)
         steps.append(res["value"])
     elapsed = time.perf_counter() - t0
     v = statistics.mean(steps)
@@ -296,8 +302,9 @@ def run_gpu(args, world, rank, local):
                    "l2": "6 distinct 132 MB weight copies, one per GEMM of a step",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak,
-                     "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": None,
-                     "kernel": "gemm_kernel<F8F8,DENSE,128,promote> at M=4096",
+                     "unit": "TFLOP/s", "frac": achieved / fp8_peak,
+                     "traffic": DOMINANT_TRAFFIC_BYTES,
+                     "kernel": DOMINANT_KERNEL,
                      "peak_source": "%s bf16 burst %.1f TFLOP/s x 2 (e4m3/bf16 nominal)"
                                     % (pk_src, pk["bf16_tflops"]),
                      "launch_ms": dom_ms},

@@ -346,7 +346,9 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------ weight producer
     if (lane == 0 && !p.inject_stall) {
-      const uint64_t pol = policy_evict_first();
+      // weights on the A side are streamed once: evict them first; tokens on
+      // the A side (token-major path) are reused by every weight tile
+      const uint64_t pol = (EPI == EPI_NORMAL) ? policy_evict_last() : policy_evict_first();
       uint32_t it = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
