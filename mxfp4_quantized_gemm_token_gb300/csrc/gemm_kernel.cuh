@@ -14,11 +14,15 @@
 //   warp 3        scale loader: per 128-wide K slice, the column scales
 //                 As(m, kb) (times the tile's Ws(kb) when it is uniform) and,
 //                 when it is not, the per-row Ws(n, kb), into a shared ring
+//                 (token-major: As of the 128 token rows and Ws of the tile's
+//                 weight blocks); the epilogue never waits on a global load
 //   warps 4..     epilogue, one or two warpgroups splitting the token columns:
 //                 TMEM -> registers, scale promotion (one FFMA per element),
 //                 output
-//   last 4 warps  (bf16 kinds only) in-shared-memory weight decode
-//                 e4m3 -> bf16 or e2m1 x 2^(e-127) -> bf16
+//   last 8 warps  (bf16 kinds only) in-shared-memory weight decode
+//                 e4m3 -> bf16 or e2m1 x 2^(e-127) -> bf16; for MXFP4 the
+//                 scale-loader warp stages each slice's ue8m0 bytes in a
+//                 shared ring ahead of the decode
 //
 // Block scales ("[XPU] block-FP8 linear via torch scaled_mm": activations
 // BlockWise1x128, weights BlockWise128x128 or 1x128) are not powers of two, so
@@ -99,7 +103,8 @@ struct Layout {
   static constexpr int EW = (KIND == KIND_F8F8 && BT >= 256) ? 4 : (BT >= 128 ? 2 : 1);
   static constexpr int COLS = BT / EW;                     // token columns per epilogue WG
   static constexpr int CONV_WARP0 = 4 + 4 * EW;
-  static constexpr int kThreads = 128 * (1 + EW + ((KIND == KIND_F8F8) ? 0 : 1));
+  static constexpr int NCV = (KIND == KIND_F8F8) ? 0 : 8;  // weight-decode warps
+  static constexpr int kThreads = 128 * (1 + EW) + 32 * NCV;
   static constexpr int A_BYTES = (KIND == KIND_MXW) ? 128 * 64 : 128 * 128;
   static constexpr int B_BYTES = BT * 128 * ((KIND == KIND_F8F8) ? 1 : 2);
   static constexpr int C_BYTES = (KIND == KIND_F8F8) ? 0 : 128 * 256;
@@ -109,6 +114,7 @@ struct Layout {
   static constexpr int GRP = kThreads >= 640 ? 16 : ((kThreads >= 512 || COLS > 64) ? 32 : COLS);
   static constexpr int OUT_BYTES = EW * STG * 128 * 4;
   static constexpr int SSLOTS = 8;                         // scale ring depth
+  static constexpr int NSTR = 160;    // token-major scale slot: 128 As + BT/128 Ws (floats)
   static constexpr int MISC_BYTES = 16384;
   static constexpr int BUDGET = 225 * 1024 - 1024;   // minus alignment slack
   static constexpr int FIXED = OUT_BYTES + MISC_BYTES + CS * C_BYTES;
@@ -126,6 +132,7 @@ struct Layout {
   static_assert(AS >= 2 && BS >= 2, "pipeline too shallow");
   static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory over budget");
   static_assert(COLS % 32 == 0 && COLS <= 128, "epilogue column split");
+  static_assert(SSLOTS * NSTR * 4 <= 8192 && SSLOTS * BT * 4 <= 8192, "scale ring size");
 };
 
 struct Unit {
@@ -297,6 +304,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* sAsc = reinterpret_cast<float*>(misc + 1024);            // [SSL][BT] column scales
   float* sWr = reinterpret_cast<float*>(misc + 1024 + 8192);      // [SSL][128] row scales
+  // MXFP4: [SSL][128] ue8m0 bytes of one slice, 4 per weight row (shares sAsc)
+  uint32_t* sMx = reinterpret_cast<uint32_t*>(misc + 1024);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -307,14 +316,14 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < AS; ++i) {
       mbar_init(&a_full[i], 1);
-      mbar_init(&a_empty[i], KIND == KIND_F8F8 ? 1 : 4);
+      mbar_init(&a_empty[i], KIND == KIND_F8F8 ? 1 : L::NCV);
     }
     for (int i = 0; i < BS; ++i) {
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < CS; ++i) {
-      mbar_init(&c_full[i], 4);
+      mbar_init(&c_full[i], L::NCV);
       mbar_init(&c_empty[i], 1);
     }
     for (int i = 0; i < NB; ++i) {
@@ -323,7 +332,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
     }
     for (int i = 0; i < SSL; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4 * EW);
+      mbar_init(&s_empty[i], KIND == KIND_MXW ? L::NCV : 4 * EW);
     }
     mbar_init(drain, 1);
     for (int g = 0; g < EW; ++g) mbar_init(&epi_bar[g], 128);
@@ -410,7 +419,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // the whole warp runs the loop; one elected lane issues
+    {
       uint32_t ia = 0, ib = 0, au = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
@@ -421,17 +431,18 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
           const bool first = (kb == U.kb0), last = (kb == U.kb1 - 1);
           const uint32_t buf = au % NB;
           if (PROMOTE || first)
-            if (!mbar_wait(&t_empty[buf], ((au / NB) & 1) ^ 1, wc)) goto mma_done;
-          const int sa = (KIND == KIND_F8F8) ? ia % AS : ia % CS;
-          if (KIND == KIND_F8F8) {
-            if (!mbar_wait(&a_full[sa], (ia / AS) & 1, wc)) goto mma_done;
-          } else {
-            if (!mbar_wait(&c_full[sa], (ia / CS) & 1, wc)) goto mma_done;
-          }
+            if (!mbar_wait_warp(&t_empty[buf], ((au / NB) & 1) ^ 1, wc)) goto mma_done;
+          // FP8 x FP8 reads the A ring; the bf16 kinds read the decoded C ring
+          constexpr int RA = (KIND == KIND_F8F8) ? AS : CS;
+          const int sa = ia % RA;
+          uint64_t* full = (KIND == KIND_F8F8) ? &a_full[sa] : &c_full[sa];
+          if (!mbar_wait_warp(full, (ia / RA) & 1, wc)) goto mma_done;
           const int sb = ib % BS;
-          if (!mbar_wait(&b_full[sb], (ib / BS) & 1, wc)) goto mma_done;
+          if (!mbar_wait_warp(&b_full[sb], (ib / BS) & 1, wc)) goto mma_done;
           tc_fence_after();
           const uint32_t d = tmem_base + buf * BT;
+          const bool leader = elect_one();
+          if (leader) {
           if (KIND == KIND_F8F8) {
             const uint32_t a0 = smem_u32(sA + sa * L::A_BYTES);
             const uint32_t b0 = smem_u32(sB + sb * L::B_BYTES);
@@ -454,17 +465,18 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
             mma_commit(&c_empty[sa]);
           }
           if (KIND != KIND_F8F8) mma_commit(&b_empty[sb]);
+          }
           ++ia;
           ++ib;
           if (PROMOTE || last) {
-            mma_commit(&t_full[buf]);
+            if (leader) mma_commit(&t_full[buf]);
             ++au;
           }
         }
       }
     mma_done:
       if (*abort_flag) {
-        mma_commit(drain);
+        if (elect_one()) mma_commit(drain);
         volatile int zero = 0;
         WaitCtx dw{p.status, &zero, 1000000000ull};
         mbar_wait(drain, 0, dw);
@@ -472,8 +484,101 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
     }
   } else if (warp == 3) {
     // ---------------------------------------------------- scale loader
-    // Two slices of look-ahead in registers hide the global-load latency.
-    if (PROMOTE && EPI != EPI_NORMAL) {
+    if (KIND == KIND_MXW) {
+      // ue8m0 bytes of each slice (4 groups of 32 along K per weight row),
+      // four slices ahead in registers; rows of a ragged tail clamp to the
+      // last row and columns past K read 127 (2^0; the data there is zero)
+      uint32_t is = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit U = get_unit<EPI, BT>(p, u);
+        uint32_t rx[4][4];
+        auto fetch = [&](int kb, uint32_t* x) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = lane + 32 * i;
+            int64_t grow = (EPI == EPI_SILU) ? static_cast<int64_t>(r < 64 ? U.wrow0 + r : U.wrow1 + (r - 64))
+                                             : static_cast<int64_t>(U.wrow0) + r;
+            if (grow >= p.mx_rows_total) grow = p.mx_rows_total - 1;
+            const uint8_t* rowp = p.mx_scale + grow * p.mx_ld;
+            uint32_t v = 0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int col = kb * 4 + c;
+              const uint32_t b = (col < p.mx_cols) ? __ldg(rowp + col) : 127u;
+              v |= b << (8 * c);
+            }
+            x[i] = v;
+          }
+        };
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (U.kb0 + q < U.kb1) fetch(U.kb0 + q, rx[q]);
+        for (int kb = U.kb0; kb < U.kb1; kb += 4) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (kb + q < U.kb1) {
+              const int slot = is % SSL;
+              if (!mbar_wait(&s_empty[slot], ((is / SSL) & 1) ^ 1, wc)) goto mx_done;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) sMx[slot * 128 + lane + 32 * i] = rx[q][i];
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&s_full[slot]);
+              ++is;
+              if (kb + q + 4 < U.kb1) fetch(kb + q + 4, rx[q]);
+            }
+          }
+        }
+      }
+    mx_done:;
+    } else if (EPI == EPI_NORMAL) {
+      // token-major: per slice, As(m, kb) of the tile's 128 token rows and
+      // Ws(blk, kb) of its BT / 128 weight blocks, four slices ahead
+      constexpr int NWB = BT / 128;
+      uint32_t is = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit U = get_unit<EPI, BT>(p, u);
+        float ra[4][4], rw[4];
+        auto fetch = [&](int kb, float* a, float& w) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = lane + 32 * i;
+            a[i] = (r < U.rows)
+                       ? __ldg(p.a_scale + static_cast<int64_t>(U.m0 + r) * p.sa0 + kb * p.sa1)
+                       : 1.f;
+          }
+          w = 1.f;
+          if (lane < NWB) {
+            const int n = U.n0 + lane * 128;
+            if (p.block_n == 0)
+              w = __ldg(p.w_scale);
+            else if (n < p.N)
+              w = __ldg(p.w_scale + static_cast<int64_t>(n / 128) * p.sw0 + kb * p.sw1);
+          }
+        };
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (U.kb0 + q < U.kb1) fetch(U.kb0 + q, ra[q], rw[q]);
+        for (int kb = U.kb0; kb < U.kb1; kb += 4) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (kb + q < U.kb1) {
+              const int slot = is % SSL;
+              if (!mbar_wait(&s_empty[slot], ((is / SSL) & 1) ^ 1, wc)) goto nscale_done;
+              float* dst = sAsc + slot * L::NSTR;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = ra[q][i];
+              if (lane < NWB) dst[128 + lane] = rw[q];
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&s_full[slot]);
+              ++is;
+              if (kb + q + 4 < U.kb1) fetch(kb + q + 4, ra[q], rw[q]);
+            }
+          }
+        }
+      }
+    nscale_done:;
+    } else if (PROMOTE) {
+      // Four slices of look-ahead in registers hide the global-load latency.
       constexpr int NA = BT / 32;
       uint32_t is = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
@@ -532,9 +637,12 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
     }
   } else if (warp >= L::CONV_WARP0) {
     // ------------------------------------------- weight decode to bf16
-    if (KIND != KIND_F8F8) {
+    // 8 warps; every thread loads all of its source chunks of the slice
+    // before converting, so the shared-memory latency overlaps.
+    if constexpr (KIND != KIND_F8F8) {
+      constexpr int CT = 32 * L::NCV;
       const int ct = threadIdx.x - 32 * L::CONV_WARP0;
-      uint32_t ia = 0, ic = 0;
+      uint32_t ia = 0, ic = 0, is = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
         for (int kb = U.kb0; kb < U.kb1; ++kb, ++ia, ++ic) {
@@ -545,43 +653,54 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
           uint8_t* dst = sC + sc * L::C_BYTES;
           if (KIND == KIND_F8W) {
             // 1024 chunks of 16 fp8 (row r, chunk c); swizzled source rows
-#pragma unroll 2
-            for (int i = 0; i < 8; ++i) {
-              const int q = i * 128 + ct;
+            constexpr int PER = 1024 / CT;
+            uint4 raw[PER];
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+              const int q = i * CT + ct;
               const int r = q >> 3, c = q & 7;
-              const uint4 raw =
-                  *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
+              raw[i] = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
+            }
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+              const int q = i * CT + ct;
+              const int r = q >> 3, c = q & 7;
               uint4 o0, o1;
-              o0.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.x));
-              o0.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.x >> 16));
-              o0.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.y));
-              o0.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.y >> 16));
-              o1.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.z));
-              o1.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.z >> 16));
-              o1.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.w));
-              o1.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw.w >> 16));
+              o0.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].x));
+              o0.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].x >> 16));
+              o0.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].y));
+              o0.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].y >> 16));
+              o1.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].z));
+              o1.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].z >> 16));
+              o1.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].w));
+              o1.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].w >> 16));
               const int h = c >> 2, cc = (c & 3) * 2;
               uint8_t* rowp = dst + h * 16384 + r * 128;
               *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = o0;
               *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ (r & 7)) << 4)) = o1;
             }
           } else {
-            // 512 chunks of 32 e2m1 (row r, 32-element group c), linear source
-#pragma unroll 1
-            for (int i = 0; i < 4; ++i) {
-              const int q = i * 128 + ct;
+            // 512 chunks of 32 e2m1 (row r, 32-element group c), linear source;
+            // the group's ue8m0 byte comes from the shared scale ring
+            constexpr int PER = 512 / CT;
+            const int slot = is % SSL;
+            if (!mbar_wait(&s_full[slot], (is / SSL) & 1, wc)) goto conv_done;
+            uint4 raw[PER];
+            uint32_t ev[PER];
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+              const int q = i * CT + ct;
+              raw[i] = *reinterpret_cast<const uint4*>(src + q * 16);
+              ev[i] = (sMx[slot * 128 + (q >> 2)] >> (8 * (q & 3))) & 0xFFu;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[slot]);
+            ++is;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+              const int q = i * CT + ct;
               const int r = q >> 2, c = q & 3;
-              const uint4 raw = *reinterpret_cast<const uint4*>(src + q * 16);
-              // ue8m0 scale of this 32-element group
-              int64_t grow;
-              if (EPI == EPI_SILU)
-                grow = static_cast<int64_t>(r < 64 ? U.wrow0 + r : U.wrow1 + (r - 64));
-              else
-                grow = static_cast<int64_t>(U.wrow0) + r;
-              if (grow >= p.mx_rows_total) grow = p.mx_rows_total - 1;
-              const int col = kb * 4 + c;
-              uint32_t e = 127;
-              if (col < p.mx_cols) e = __ldg(p.mx_scale + grow * p.mx_ld + col);
+              const uint32_t e = ev[i];
               // bf16 2^(e - 127 + 112) when representable; else two steps
               __nv_bfloat162 sc2;
               uint32_t two_step = 0;
@@ -597,7 +716,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
                 }
               }
               uint32_t w[16];
-              const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
+              const uint32_t in[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
 #pragma unroll
@@ -645,27 +764,25 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
     const int et = (threadIdx.x - 128) & 127;
     const int col0 = g * COLS;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t au = 0;
+    uint32_t au = 0, is = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit U = get_unit<EPI, BT>(p, u);
       const bool mrow = et < U.rows;
-      const int m = U.m0 + (mrow ? et : 0);
       const int ncv = min(BT, p.N - U.n0);              // valid weight columns of the tile
       const int colv = max(0, min(COLS, ncv - col0));
       const int ngr = (colv + GRP - 1) / GRP;
-      const int64_t wblk = (U.n0 + col0) / 128;
-      const float* arow = p.a_scale + static_cast<int64_t>(m) * p.sa0;
-      auto scale_at = [&](int kb) -> float {
-        const float w = (p.block_n == 0) ? __ldg(p.w_scale) : __ldg(p.w_scale + wblk * p.sw0 + kb * p.sw1);
-        return __ldg(arow + kb * p.sa1) * w;
-      };
+      const int wsel = col0 / 128;                       // weight block of this WG's columns
       float acc[COLS];
 #pragma unroll
       for (int j = 0; j < COLS; ++j) acc[j] = 0.f;
-      float sc_nx = scale_at(U.kb0);
       for (int kb = U.kb0; kb < U.kb1; ++kb) {
-        const float sc = sc_nx;
-        if (kb + 1 < U.kb1) sc_nx = scale_at(kb + 1);
+        // slice scale As(m, kb) * Ws(blk, kb), staged by the scale loader
+        const int slot = is % SSL;
+        if (!mbar_wait(&s_full[slot], (is / SSL) & 1, wc)) goto epin_done;
+        const float sc = sAsc[slot * L::NSTR + et] * sAsc[slot * L::NSTR + 128 + wsel];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[slot]);
+        ++is;
         const uint32_t buf = au % NB;
         if (!mbar_wait(&t_full[buf], (au / NB) & 1, wc)) goto epin_done;
         tc_fence_after();

@@ -295,6 +295,24 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// mbar_wait run by every lane of a warp, with a warp-uniform result: if any
+// lane gave up, all return false (the lanes reconverge here, so code after
+// it may use warp-collective instructions).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  const bool ok = mbar_wait(bar, parity, w);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// One lane of the (converged) warp returns true.  Issuing tcgen05.mma from
+// warp-uniform control flow under this predicate keeps the descriptors in
+// uniform registers; a loop run by lane 0 alone issues measurably slower.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{ .reg .pred P; elect.sync _|P, 0xffffffff; selp.u32 %0, 1, 0, P; }"
+               : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
