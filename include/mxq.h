@@ -75,8 +75,10 @@ enum {
   MXQ_OPT_INJECT_STALL = 5, /* TEST ONLY: GEMM producers issue no copy, so every
                                consumer wait runs out (exercises MXQ_ERR_TIMEOUT) */
   MXQ_OPT_NUM_SMS = 6,      /* persistent grid size cap; 0 = all SMs */
-  MXQ_OPT_TILE_N = 7        /* fp8_scaled_mm token-tile width: 0 auto, or 32, 64, 128,
+  MXQ_OPT_TILE_N = 7,       /* fp8_scaled_mm token-tile width: 0 auto, or 32, 64, 128,
                                256 (256 for FP8 activations only) */
+  MXQ_OPT_NORMAL_TILE = 8   /* fp8_scaled_mm weight-tile width when the tokens sit on
+                               the MMA M side (large-M W8A8): 0 auto, 128, 192 or 256 */
 };
 
 const char* mxq_last_error(void);

@@ -29,7 +29,7 @@ mxq_status cuda_fail(cudaError_t e, const char* what) {
   return fail(MXQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-std::atomic<int64_t> g_opts[8] = {0, int64_t(1) << 30, 0, 2000000000LL, 0, 0, 0, 0};
+std::atomic<int64_t> g_opts[9] = {0, int64_t(1) << 30, 0, 2000000000LL, 0, 0, 0, 0, 0};
 
 std::mutex g_dev_mu;
 DeviceInfo g_devs[64];
@@ -48,7 +48,7 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 void set_last_error(const std::string& msg) { g_err = msg; }
 
 int64_t option(int32_t which) {
-  if (which < 0 || which >= 8) return 0;
+  if (which < 0 || which >= static_cast<int32_t>(sizeof(g_opts) / sizeof(g_opts[0]))) return 0;
   return g_opts[which].load();
 }
 
@@ -132,8 +132,10 @@ extern "C" const char* mxq_last_error(void) { return g_err.c_str(); }
 extern "C" const char* mxq_version(void) { return "mxq 0.1 (sm_103a, tcgen05)"; }
 
 extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
-  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_TILE_N)
+  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_NORMAL_TILE)
     return fail(MXQ_ERR_INVALID_ARG, "unknown option " + std::to_string(opt));
+  if (opt == MXQ_OPT_NORMAL_TILE && value != 0 && value != 128 && value != 192 && value != 256)
+    return fail(MXQ_ERR_INVALID_ARG, "NORMAL_TILE is 0 (auto), 128, 192 or 256");
   if (opt == MXQ_OPT_TILE_N && value != 0 && value != 32 && value != 64 && value != 128 &&
       value != 256)
     return fail(MXQ_ERR_INVALID_ARG, "TILE_N is 0 (auto), 32, 64, 128 or 256");
@@ -145,7 +147,7 @@ extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
 }
 
 extern "C" mxq_status mxq_get_option(int32_t opt, int64_t* value) {
-  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_TILE_N || value == nullptr)
+  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_NORMAL_TILE || value == nullptr)
     return fail(MXQ_ERR_INVALID_ARG, "unknown option or NULL value");
   *value = g_opts[opt].load();
   return MXQ_OK;
@@ -217,7 +219,14 @@ MmPlan plan_mm(int64_t M, int64_t N, int64_t K, int32_t a_dtype, bool block, boo
   // Large M with a weight scale that is uniform over 128 weight rows: put the
   // tokens on the MMA M side so each TMEM lane's slice scale is one scalar.
   pl.normal = pl.kind == KIND_F8F8 && has_ascale && uniform_wscale && M > 128 && tile == 0;
-  if (pl.normal) pl.bt = (M >= 512 && N >= 4096) ? 256 : 128;
+  if (pl.normal) {
+    const int64_t nt = option(MXQ_OPT_NORMAL_TILE);
+    // 192-wide weight tiles keep the epilogue's 64 accumulators per thread
+    // clear of spills (512 threads); 256 packs fewer waves when the token
+    // count is small
+    pl.bt = nt > 0 ? static_cast<int>(nt)
+                   : (N < 4096 ? 128 : (M >= 2048 ? 192 : (M >= 512 ? 256 : 128)));
+  }
   pl.promote = block || has_ascale;
   pl.tiles_n = static_cast<int>(cdiv(N, pl.normal ? pl.bt : 128));
   pl.tiles_m = static_cast<int>(cdiv(M, pl.normal ? 128 : pl.bt));

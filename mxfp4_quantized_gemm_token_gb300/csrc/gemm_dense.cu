@@ -13,6 +13,8 @@ cudaError_t launch_gemm(int kind, int epi, int bt, bool promote, const GemmMaps&
     // tokens on the MMA M side: FP8 x FP8 with uniform weight-block scales
     if (kind == KIND_F8F8 && bt == 128)
       return launch_gemm_inst<KIND_F8F8, EPI_NORMAL, 128, true>(maps, p, grid, stream);
+    if (kind == KIND_F8F8 && bt == 192)
+      return launch_gemm_inst<KIND_F8F8, EPI_NORMAL, 192, true>(maps, p, grid, stream);
     if (kind == KIND_F8F8 && bt == 256)
       return launch_gemm_inst<KIND_F8F8, EPI_NORMAL, 256, true>(maps, p, grid, stream);
     return cudaErrorInvalidValue;

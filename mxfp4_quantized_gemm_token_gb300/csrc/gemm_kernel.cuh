@@ -99,8 +99,9 @@ struct GemmParams {
 
 template <int KIND, int BT>
 struct Layout {
-  // epilogue warpgroups (one for up to 64 token columns, else two)
-  static constexpr int EW = (KIND == KIND_F8F8 && BT >= 256) ? 4 : (BT >= 128 ? 2 : 1);
+  // epilogue warpgroups: one for up to 64 columns, two for 128; FP8 x FP8
+  // tiles of 192 / 256 columns use three / four (64 columns each)
+  static constexpr int EW = (KIND == KIND_F8F8 && BT >= 192) ? BT / 64 : (BT >= 128 ? 2 : 1);
   static constexpr int COLS = BT / EW;                     // token columns per epilogue WG
   static constexpr int CONV_WARP0 = 4 + 4 * EW;
   static constexpr int NCV = (KIND == KIND_F8F8) ? 0 : 8;  // weight-decode warps
@@ -127,8 +128,11 @@ struct Layout {
   static constexpr int AS = AS_RAW > 12 ? 12 : AS_RAW;
   static constexpr int BS = (KIND == KIND_F8F8) ? AS : BS_PREF;
   static constexpr int TOTAL = AS * A_BYTES + CS * C_BYTES + BS * B_BYTES + OUT_BYTES + MISC_BYTES;
-  static constexpr int NBUF = BT >= 256 ? 2 : 4;           // TMEM accumulator buffers
-  static constexpr int TMEM_COLS = NBUF * BT;
+  static constexpr int NBUF = BT > 128 ? 2 : 4;            // TMEM accumulator buffers
+  // each accumulator starts at a power-of-two column offset (192-wide tiles
+  // take 256-column slots); the allocation is a power of two
+  static constexpr int BSTRIDE = BT > 128 ? 256 : BT;
+  static constexpr int TMEM_COLS = NBUF * BSTRIDE;
   static_assert(AS >= 2 && BS >= 2, "pipeline too shallow");
   static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory over budget");
   static_assert(COLS % 32 == 0 && COLS <= 128, "epilogue column split");
@@ -147,7 +151,8 @@ struct Unit {
   int wrow0, wrow1;   // TMA row coordinates of the MMA-A box(es)
   int brow;           // TMA row coordinate of the MMA-B box
   int n_inst;   // MMA instruction N
-  int bvar;     // token box variant (rows 16 << bvar)
+  int bvar;     // MMA-B box variant (maps.b[bvar])
+  int brows;    // rows of that box
 };
 
 __device__ __forceinline__ int box_variant(int n) {
@@ -169,6 +174,7 @@ __device__ __forceinline__ Unit get_unit(const GemmParams& p, int u) {
     U.blk = 0;
     U.n_inst = BT;
     U.bvar = box_variant(BT);
+    U.brows = BT;
     if (EPI == EPI_NORMAL) {
       // 128 tokens (A, TMEM lanes) x BT weight rows (B, TMEM columns)
       U.n0 = U.tn * BT;
@@ -209,6 +215,7 @@ __device__ __forceinline__ Unit get_unit(const GemmParams& p, int u) {
     const int fit = ((U.rows + 15) / 16) * 16;
     U.n_inst = (U.rows <= p.narrow_max) ? min(fit, BT) : BT;
     U.bvar = box_variant(U.n_inst);
+    U.brows = 16 << U.bvar;
     U.brow = U.m0;
   }
   return U;
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
       uint32_t it = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
-        const int brows = 16 << U.bvar;
+        const int brows = U.brows;
         const CUtensorMap* mb = &maps.b[U.bvar];
         for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
           const int s = it % BS;
@@ -424,7 +431,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
       uint32_t ia = 0, ib = 0, au = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
-        const int brows = 16 << U.bvar;
+        const int brows = U.brows;
         const uint32_t idesc =
             (KIND == KIND_F8F8) ? idesc_e4m3(128, U.n_inst) : idesc_bf16(128, U.n_inst);
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
@@ -440,7 +447,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
           const int sb = ib % BS;
           if (!mbar_wait_warp(&b_full[sb], (ib / BS) & 1, wc)) goto mma_done;
           tc_fence_after();
-          const uint32_t d = tmem_base + buf * BT;
+          const uint32_t d = tmem_base + buf * L::BSTRIDE;
           const bool leader = elect_one();
           if (leader) {
           if (KIND == KIND_F8F8) {
@@ -533,7 +540,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
     } else if (EPI == EPI_NORMAL) {
       // token-major: per slice, As(m, kb) of the tile's 128 token rows and
       // Ws(blk, kb) of its BT / 128 weight blocks, four slices ahead
-      constexpr int NWB = BT / 128;
+      constexpr int NWB = (BT + 127) / 128 + (BT % 128 != 0 ? 1 : 0);   // weight blocks a tile can span
       uint32_t is = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
@@ -548,7 +555,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
           }
           w = 1.f;
           if (lane < NWB) {
-            const int n = U.n0 + lane * 128;
+            const int n = (U.n0 / 128 + lane) * 128;
             if (p.block_n == 0)
               w = __ldg(p.w_scale);
             else if (n < p.N)
@@ -771,7 +778,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
       const int ncv = min(BT, p.N - U.n0);              // valid weight columns of the tile
       const int colv = max(0, min(COLS, ncv - col0));
       const int ngr = (colv + GRP - 1) / GRP;
-      const int wsel = col0 / 128;                       // weight block of this WG's columns
+      // weight block of this WG's 64 columns (64-aligned, so inside one block)
+      const int wsel = (U.n0 + col0) / 128 - U.n0 / 128;
       float acc[COLS];
 #pragma unroll
       for (int j = 0; j < COLS; ++j) acc[j] = 0.f;
@@ -791,7 +799,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
         for (int c = 0; c < COLS / GRP; ++c) {
           if (c < ngr) {
             float v[GRP];
-            tmem_ld<GRP>(tmem_base + lane_addr + buf * BT + col0 + c * GRP, v);
+            tmem_ld<GRP>(tmem_base + lane_addr + buf * L::BSTRIDE + col0 + c * GRP, v);
             if (c == COLS / GRP - 1 || c + 1 == ngr) {
               tc_fence_before();
               __syncwarp();
@@ -897,7 +905,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
           for (int c = 0; c < COLS / GRP; ++c) {
             if (c < ngr) {
               float v[GRP];
-              tmem_ld<GRP>(tmem_base + lane_addr + buf * BT + col0 + c * GRP, v);
+              tmem_ld<GRP>(tmem_base + lane_addr + buf * L::BSTRIDE + col0 + c * GRP, v);
               if (c == COLS / GRP - 1 || c + 1 == ngr) {
                 // the last TMEM read of this slice is done: hand the buffer
                 // back to the MMA before doing the arithmetic
@@ -947,7 +955,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < COLS / GRP; ++c) {
-          if (c < ngr) tmem_ld<GRP>(tmem_base + lane_addr + buf * BT + col0 + c * GRP, &acc[c * GRP]);
+          if (c < ngr) tmem_ld<GRP>(tmem_base + lane_addr + buf * L::BSTRIDE + col0 + c * GRP, &acc[c * GRP]);
         }
         tc_fence_before();
         __syncwarp();

@@ -29,7 +29,7 @@ def block_case(oracle, M, N, K, block_n, seed, bias=None, x=None):
     o32 = mxq.fp8_scaled_mm(q, wq.cuda(), ws.cuda(), [block_n, 128], a_scale=s, bias=bc,
                             out_dtype=torch.float32)
     o16 = mxq.fp8_scaled_mm(q, wq.cuda(), ws.cuda(), [block_n, 128], a_scale=s, bias=bc)
-    torch.cuda.synchronize()
+    mxq.sync_status()
     assert_probe_close(o32, rf)
     assert_bf16_close(o16, rb)
     return o32, o16
@@ -203,6 +203,21 @@ def test_full_size_block1x128_sampled_rows(oracle, M):
     rq, rs = oracle.per_token_group_quant_fp8(bits16(xf[ridx]), 128)
     _, rb = oracle.scaled_mm(rq, E4M3, rs, u8(wq), ws.cpu().numpy(), 1, 128)
     assert_bf16_close(flat[ridx], rb)
+
+
+@pytest.mark.parametrize("tile", [128, 192, 256])
+def test_token_major_tile_widths(oracle, tile):
+    """Every weight-tile width of the token-major path (tokens on the MMA M
+    side) on ragged shapes: partial last token and weight tiles, 192-wide
+    tiles that start inside a 128-row weight block, bias, bf16 and f32 out."""
+    try:
+        mxq.set_option(_lib.OPT_NORMAL_TILE, tile)
+        block_case(oracle, 300, 384, 640, 128, seed=61 + tile)
+        block_case(oracle, 260, 704, 512, 128, seed=62 + tile,
+                   bias=torch.randn(704, generator=torch.Generator().manual_seed(tile)))
+        block_case(oracle, 129, 640, 384, 128, seed=63 + tile)
+    finally:
+        mxq.set_option(_lib.OPT_NORMAL_TILE, 0)
 
 
 @pytest.mark.parametrize("tile", [32, 64, 128, 256])
