@@ -8,9 +8,13 @@
 // code serves large token counts with BT = 128.
 //
 // Warp roles (one CTA per SM, persistent over work units):
-//   warp 0        TMA producer for the weight operand (A ring)
-//   warp 1        TMEM allocator + single-thread tcgen05.mma issuer
-//   warp 2        TMA producer for the token operand (B ring)
+//   warp 0        TMA producer for the weight operand (A ring); for FP8 x FP8
+//                 it also loads the B operand of the same slice
+//   warp 1        TMEM allocator + tcgen05.mma issuer (one elected lane)
+//   warp 2        TMA producer for the B operand (bf16 kinds), or for
+//                 FP8 x FP8 a second MMA issuer: warps 1 and 2 take the even
+//                 and odd K slices (each slice has its own TMEM buffer), so
+//                 one warp's barrier waits never leave the tensor pipe idle
 //   warp 3        scale loader: per 128-wide K slice, the column scales
 //                 As(m, kb) (times the tile's Ws(kb) when it is uniform) and,
 //                 when it is not, the per-row Ws(n, kb), into a shared ring
@@ -97,7 +101,7 @@ struct GemmParams {
   int vec_ok;
 };
 
-template <int KIND, int BT>
+template <int KIND, int BT, int EPI>
 struct Layout {
   // epilogue warpgroups: one for up to 64 columns, two for 128; FP8 x FP8
   // tiles of 192 / 256 columns use three / four (64 columns each)
@@ -111,9 +115,14 @@ struct Layout {
   static constexpr int C_BYTES = (KIND == KIND_F8F8) ? 0 : 128 * 256;
   static constexpr int CS = (KIND == KIND_F8F8) ? 0 : 2;
   static constexpr int STG = EW >= 4 ? 8 : 16;             // token columns staged per pass
-  // TMEM columns loaded per wait (bounded by registers: acc + one group live)
-  static constexpr int GRP = kThreads >= 640 ? 16 : ((kThreads >= 512 || COLS > 64) ? 32 : COLS);
-  static constexpr int OUT_BYTES = EW * STG * 128 * 4;
+  // TMEM columns loaded per wait (bounded by registers: acc + one group
+  // live).  The token-major epilogue at 512 threads reads its 64 columns with
+  // one wait, so the accumulator buffer goes back to the MMA before any FMA.
+  static constexpr int GRP = (EPI == EPI_NORMAL && kThreads == 512)
+                                 ? 64
+                                 : (kThreads >= 640 ? 16 : ((kThreads >= 512 || COLS > 64) ? 32 : COLS));
+  // output staging of the weight-major epilogue (the token-major one stores directly)
+  static constexpr int OUT_BYTES = (EPI == EPI_NORMAL) ? 0 : EW * STG * 128 * 4;
   static constexpr int SSLOTS = 8;                         // scale ring depth
   static constexpr int NSTR = 160;    // token-major scale slot: 128 As + BT/128 Ws (floats)
   static constexpr int MISC_BYTES = 16384;
@@ -281,9 +290,10 @@ __device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, const
 
 // ------------------------------------------------------------------ kernel
 template <int KIND, int EPI, int BT, bool PROMOTE>
-__global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
+__global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  using L = Layout<KIND, BT>;
+  using L = Layout<KIND, BT, EPI>;
+  static_assert(KIND != KIND_F8F8 || PROMOTE, "FP8 x FP8 slices are always promoted (two issuers rely on it)");
   constexpr int AS = L::AS, BS = L::BS, CS = L::CS, EW = L::EW, COLS = L::COLS;
   constexpr int SSL = L::SSLOTS, STG = L::STG, GRP = L::GRP, NB = L::NBUF;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -305,8 +315,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
   uint64_t* t_empty = t_full + 4;
   uint64_t* s_full = t_empty + 4;
   uint64_t* s_empty = s_full + SSL;
-  uint64_t* drain = s_empty + SSL;
-  uint64_t* epi_bar = drain + 1;     // bounded barriers, one per epilogue warpgroup
+  uint64_t* drain = s_empty + SSL;   // one per MMA issuer
+  uint64_t* epi_bar = drain + 2;     // bounded barriers, one per epilogue warpgroup
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 4);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* sAsc = reinterpret_cast<float*>(misc + 1024);            // [SSL][BT] column scales
@@ -341,7 +351,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], KIND == KIND_MXW ? L::NCV : 4 * EW);
     }
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     for (int g = 0; g < EW; ++g) mbar_init(&epi_bar[g], 128);
     *abort_flag = 0;
     fence_barrier_init();
@@ -371,9 +382,15 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
         for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
           const int s = it % AS;
           if (!mbar_wait(&a_empty[s], ((it / AS) & 1) ^ 1, wc)) goto prod_a_done;
-          mbar_expect_tx(&a_full[s], L::A_BYTES);
           const int kc = (KIND == KIND_MXW) ? kb * 64 : kb * 128;
           uint8_t* dst = sA + s * L::A_BYTES;
+          if (KIND == KIND_F8F8) {
+            // FP8 x FP8: both operands of the slice land on one barrier
+            mbar_expect_tx(&a_full[s], L::A_BYTES + U.brows * 128);
+            tma_load_2d(sB + s * L::B_BYTES, &maps.b[U.bvar], &a_full[s], kb * 128, U.brow);
+          } else {
+            mbar_expect_tx(&a_full[s], L::A_BYTES);
+          }
           if (EPI == EPI_SILU) {
             tma_load_2d_hint(dst, &maps.a, &a_full[s], kc, U.wrow0, pol);
             tma_load_2d_hint(dst + L::A_BYTES / 2, &maps.a, &a_full[s], kc, U.wrow1, pol);
@@ -391,7 +408,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
         for (uint32_t i = first; i < it; ++i) mbar_wait(&a_full[i % AS], (i / AS) & 1, dw);
       }
     }
-  } else if (warp == 2) {
+  } else if (warp == 2 && KIND != KIND_F8F8) {
     // ------------------------------------------------- token producer
     if (lane == 0 && !p.inject_stall) {
       uint32_t it = 0;
@@ -424,10 +441,13 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
         for (uint32_t i = first; i < it; ++i) mbar_wait(&b_full[i % BS], (i / BS) & 1, dw);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (KIND == KIND_F8F8 && warp == 2)) {
     // ------------------------------------------------------ MMA issuer
-    // the whole warp runs the loop; one elected lane issues
+    // the whole warp runs the loop; one elected lane issues.  FP8 x FP8 has
+    // two issuing warps, each taking every other slice.
     {
+      constexpr uint32_t NISS = (KIND == KIND_F8F8) ? 2 : 1;
+      const uint32_t mine = static_cast<uint32_t>(warp - 1);
       uint32_t ia = 0, ib = 0, au = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
@@ -436,6 +456,14 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
             (KIND == KIND_F8F8) ? idesc_e4m3(128, U.n_inst) : idesc_bf16(128, U.n_inst);
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
           const bool first = (kb == U.kb0), last = (kb == U.kb1 - 1);
+          if (NISS > 1 && ia % NISS != mine) {
+            // the other issuer's slice (F8F8 slices are always promoted,
+            // so every slice advances every counter)
+            ++ia;
+            ++ib;
+            ++au;
+            continue;
+          }
           const uint32_t buf = au % NB;
           if (PROMOTE || first)
             if (!mbar_wait_warp(&t_empty[buf], ((au / NB) & 1) ^ 1, wc)) goto mma_done;
@@ -445,7 +473,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
           uint64_t* full = (KIND == KIND_F8F8) ? &a_full[sa] : &c_full[sa];
           if (!mbar_wait_warp(full, (ia / RA) & 1, wc)) goto mma_done;
           const int sb = ib % BS;
-          if (!mbar_wait_warp(&b_full[sb], (ib / BS) & 1, wc)) goto mma_done;
+          if (KIND != KIND_F8F8)
+            if (!mbar_wait_warp(&b_full[sb], (ib / BS) & 1, wc)) goto mma_done;
           tc_fence_after();
           const uint32_t d = tmem_base + buf * L::BSTRIDE;
           const bool leader = elect_one();
@@ -483,10 +512,11 @@ __global__ void __launch_bounds__(Layout<KIND, BT>::kThreads, 1)
       }
     mma_done:
       if (*abort_flag) {
-        if (elect_one()) mma_commit(drain);
+        // each issuer waits for its own MMAs before the TMEM is freed
+        if (elect_one()) mma_commit(&drain[mine]);
         volatile int zero = 0;
         WaitCtx dw{p.status, &zero, 1000000000ull};
-        mbar_wait(drain, 0, dw);
+        mbar_wait(&drain[mine], 0, dw);
       }
     }
   } else if (warp == 3) {

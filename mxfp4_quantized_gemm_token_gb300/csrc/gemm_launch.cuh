@@ -8,7 +8,7 @@ namespace mxq {
 template <int KIND, int EPI, int BT, bool PROMOTE>
 cudaError_t launch_gemm_inst(const GemmMaps& maps, const GemmParams& p, int grid,
                              cudaStream_t stream) {
-  using L = Layout<KIND, BT>;
+  using L = Layout<KIND, BT, EPI>;
   const int smem = L::TOTAL + 1024;
   static int configured[64] = {0};
   int dev = 0;
