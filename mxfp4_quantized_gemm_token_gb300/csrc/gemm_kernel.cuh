@@ -11,11 +11,12 @@
 //   warp 0        TMA producer for the weight operand (A ring); for FP8 x FP8
 //                 it also loads the B operand of the same slice
 //   warp 1        TMEM allocator + tcgen05.mma issuer (one elected lane)
-//   warp 2        TMA producer for the B operand (bf16 kinds), or for
-//                 FP8 x FP8 a second MMA issuer: warps 1 and 2 take the even
-//                 and odd K slices (each slice has its own TMEM buffer), so
-//                 one warp's barrier waits never leave the tensor pipe idle
-//   warp 3        scale loader: per 128-wide K slice, the column scales
+//   warp 2        with per-slice promotion, a second MMA issuer: warps 1
+//                 and 2 take the even and odd K slices (each slice has its
+//                 own TMEM buffer), so one warp's barrier waits never leave
+//                 the tensor pipe idle
+//   warp 3        bf16 kinds: TMA producer for the B operand (bf16 tokens);
+//                 scale loader: per 128-wide K slice, the column scales
 //                 As(m, kb) (times the tile's Ws(kb) when it is uniform) and,
 //                 when it is not, the per-row Ws(n, kb), into a shared ring
 //                 (token-major: As of the 128 token rows and Ws of the tile's
@@ -408,45 +409,13 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         for (uint32_t i = first; i < it; ++i) mbar_wait(&a_full[i % AS], (i / AS) & 1, dw);
       }
     }
-  } else if (warp == 2 && KIND != KIND_F8F8) {
-    // ------------------------------------------------- token producer
-    if (lane == 0 && !p.inject_stall) {
-      uint32_t it = 0;
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const Unit U = get_unit<EPI, BT>(p, u);
-        const int brows = U.brows;
-        const CUtensorMap* mb = &maps.b[U.bvar];
-        for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
-          const int s = it % BS;
-          // FP8 x FP8: A and B stages advance together and are released by
-          // one commit (a_empty); the bf16 kinds release B on its own ring
-          uint64_t* rel = (KIND == KIND_F8F8) ? &a_empty[s] : &b_empty[s];
-          if (!mbar_wait(rel, ((it / BS) & 1) ^ 1, wc)) goto prod_b_done;
-          uint8_t* dst = sB + s * L::B_BYTES;
-          if (KIND == KIND_F8F8) {
-            mbar_expect_tx(&b_full[s], brows * 128);
-            tma_load_2d(dst, mb, &b_full[s], kb * 128, U.brow);
-          } else {
-            mbar_expect_tx(&b_full[s], brows * 256);
-            tma_load_2d(dst, mb, &b_full[s], kb * 128, U.brow);
-            tma_load_2d(dst + brows * 128, mb, &b_full[s], kb * 128 + 64, U.brow);
-          }
-        }
-      }
-    prod_b_done:
-      if (*abort_flag) {
-        volatile int zero = 0;
-        WaitCtx dw{p.status, &zero, 1000000000ull};
-        const uint32_t first = it > static_cast<uint32_t>(BS) ? it - BS : 0;
-        for (uint32_t i = first; i < it; ++i) mbar_wait(&b_full[i % BS], (i / BS) & 1, dw);
-      }
-    }
-  } else if (warp == 1 || (KIND == KIND_F8F8 && warp == 2)) {
+  } else if (warp == 1 || (PROMOTE && warp == 2)) {
     // ------------------------------------------------------ MMA issuer
-    // the whole warp runs the loop; one elected lane issues.  FP8 x FP8 has
-    // two issuing warps, each taking every other slice.
+    // the whole warp runs the loop; one elected lane issues.  With per-slice
+    // promotion every slice has its own TMEM buffer and two issuing warps
+    // take every other slice.
     {
-      constexpr uint32_t NISS = (KIND == KIND_F8F8) ? 2 : 1;
+      constexpr uint32_t NISS = PROMOTE ? 2 : 1;
       const uint32_t mine = static_cast<uint32_t>(warp - 1);
       uint32_t ia = 0, ib = 0, au = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
@@ -457,8 +426,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
           const bool first = (kb == U.kb0), last = (kb == U.kb1 - 1);
           if (NISS > 1 && ia % NISS != mine) {
-            // the other issuer's slice (F8F8 slices are always promoted,
-            // so every slice advances every counter)
+            // the other issuer's slice (promoted: every slice advances
+            // every counter)
             ++ia;
             ++ib;
             ++au;
@@ -520,8 +489,36 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       }
     }
   } else if (warp == 3) {
-    // ---------------------------------------------------- scale loader
-    if (KIND == KIND_MXW) {
+    // ------------------------------------- scale loader (+ bf16 B operand)
+    // bf16 kinds: this warp also loads the B operand (bf16 tokens, two
+    // 64-column halves) of every slice, in slice order, just before
+    // publishing the slice's scales; the B ring is released by the MMA
+    uint32_t itb = 0;
+    auto produce_b = [&](const Unit& U, int kb) -> bool {
+      if (KIND == KIND_F8F8) return true;
+      if (!p.inject_stall) {
+        const int sb = itb % BS;
+        if (!mbar_wait(&b_empty[sb], ((itb / BS) & 1) ^ 1, wc)) return false;
+        if (lane == 0) {
+          uint8_t* dst = sB + sb * L::B_BYTES;
+          const CUtensorMap* mb = &maps.b[U.bvar];
+          mbar_expect_tx(&b_full[sb], U.brows * 256);
+          tma_load_2d(dst, mb, &b_full[sb], kb * 128, U.brow);
+          tma_load_2d(dst + U.brows * 128, mb, &b_full[sb], kb * 128 + 64, U.brow);
+        }
+        __syncwarp();
+      }
+      ++itb;
+      return true;
+    };
+    if (KIND == KIND_F8W && !PROMOTE) {
+      // per-tensor weights: no slice scales, only the B operand
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit U = get_unit<EPI, BT>(p, u);
+        for (int kb = U.kb0; kb < U.kb1; ++kb)
+          if (!produce_b(U, kb)) goto scale_done;
+      }
+    } else if (KIND == KIND_MXW) {
       // ue8m0 bytes of each slice (4 groups of 32 along K per weight row),
       // four slices ahead in registers; rows of a ragged tail clamp to the
       // last row and columns past K read 127 (2^0; the data there is zero)
@@ -554,6 +551,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             if (kb + q < U.kb1) {
+              if (!produce_b(U, kb + q)) goto mx_done;
               const int slot = is % SSL;
               if (!mbar_wait(&s_empty[slot], ((is / SSL) & 1) ^ 1, wc)) goto mx_done;
 #pragma unroll
@@ -664,13 +662,21 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             if (kb + q < U.kb1) {
+              if (!produce_b(U, kb + q)) goto scale_done;
               if (!publish(ra[q], rw[q], ru[q])) goto scale_done;
               if (kb + q + 4 < U.kb1) fetch(kb + q + 4, ra[q], rw[q], ru[q]);
             }
           }
         }
       }
-    scale_done:;
+    }
+  scale_done:
+    if (KIND != KIND_F8F8 && *abort_flag && !p.inject_stall) {
+      // let every B copy already issued land before the CTA goes away
+      volatile int zero = 0;
+      WaitCtx dw{p.status, &zero, 1000000000ull};
+      const uint32_t first = itb > static_cast<uint32_t>(BS) ? itb - BS : 0;
+      for (uint32_t i = first; i < itb; ++i) mbar_wait(&b_full[i % BS], (i / BS) & 1, dw);
     }
   } else if (warp >= L::CONV_WARP0) {
     // ------------------------------------------- weight decode to bf16
