@@ -531,8 +531,10 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
                        CU_TENSOR_MAP_SWIZZLE_128B, &err))
         return fail(MXQ_ERR_CUDA, err);
     } else {
+      // 64-byte swizzle: the decode threads (one per weight row) read
+      // 16-byte chunks of 64-byte rows without bank conflicts
       if (!make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, wt, red / 2, E * rows, red / 2, 64,
-                       arows, CU_TENSOR_MAP_SWIZZLE_NONE, &err))
+                       arows, CU_TENSOR_MAP_SWIZZLE_64B, &err))
         return fail(MXQ_ERR_CUDA, err);
     }
     for (int v = 0; v < 4; ++v) {

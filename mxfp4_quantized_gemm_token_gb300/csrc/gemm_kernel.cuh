@@ -24,15 +24,17 @@
 //   warps 4..     epilogue, one or two warpgroups splitting the token columns:
 //                 TMEM -> registers, scale promotion (one FFMA per element),
 //                 output
-//   last 8 warps  (bf16 kinds only) in-shared-memory weight decode
-//                 e4m3 -> bf16 or e2m1 x 2^(e-127) -> bf16; for MXFP4 the
-//                 scale-loader warp stages each slice's ue8m0 bytes in a
-//                 shared ring ahead of the decode
+//   last 8 warps  (bf16 kinds only) weight decode, one thread per weight
+//                 row: e4m3 -> bf16 or e2m1 x 2^(e-127) -> bf16 from the
+//                 shared tile into a 4-slot TMEM ring that the MMA reads as
+//                 its A operand (no bf16 copy of the weights in shared
+//                 memory); for MXFP4 the scale warp stages each slice's ue8m0
+//                 bytes in a shared ring ahead of the decode
 //
 // Block scales ("[XPU] block-FP8 linear via torch scaled_mm": activations
 // BlockWise1x128, weights BlockWise128x128 or 1x128) are not powers of two, so
 // they cannot ride the hardware block-scaled MMA.  Instead each 128-wide K
-// slice is accumulated into its own TMEM buffer (two buffers, ping-pong) and
+// slice is accumulated into its own TMEM buffer (a ring of two to four) and
 // the epilogue folds it into fp32 registers with the slice's scale product:
 //   acc[n, m] += Ws(n, kb) * As(m, kb) * partial_kb[n, m]
 // which is the definition of the scaled product evaluated slice by slice.
@@ -113,8 +115,10 @@ struct Layout {
   static constexpr int kThreads = 128 * (1 + EW) + 32 * NCV;
   static constexpr int A_BYTES = (KIND == KIND_MXW) ? 128 * 64 : 128 * 128;
   static constexpr int B_BYTES = BT * 128 * ((KIND == KIND_F8F8) ? 1 : 2);
-  static constexpr int C_BYTES = (KIND == KIND_F8F8) ? 0 : 128 * 256;
-  static constexpr int CS = (KIND == KIND_F8F8) ? 0 : 2;
+  // bf16 kinds: decoded weight slices (128 rows x 128 K bf16 = 64 TMEM
+  // columns each) live in a TMEM ring and feed the MMA's A operand directly
+  static constexpr int CS = (KIND == KIND_F8F8) ? 0 : 4;
+  static constexpr int C_TCOL = 256;                       // first column of that ring
   static constexpr int STG = EW >= 4 ? 8 : 16;             // token columns staged per pass
   // TMEM columns loaded per wait (bounded by registers: acc + one group
   // live).  The token-major epilogue at 512 threads reads its 64 columns with
@@ -128,7 +132,7 @@ struct Layout {
   static constexpr int NSTR = 160;    // token-major scale slot: 128 As + BT/128 Ws (floats)
   static constexpr int MISC_BYTES = 16384;
   static constexpr int BUDGET = 225 * 1024 - 1024;   // minus alignment slack
-  static constexpr int FIXED = OUT_BYTES + MISC_BYTES + CS * C_BYTES;
+  static constexpr int FIXED = OUT_BYTES + MISC_BYTES;
   // F8F8: A and B stages in lock step; bf16 kinds: B ring 4 deep when it fits
   static constexpr int BS_PREF =
       (KIND == KIND_F8F8) ? 0 : (B_BYTES * 4 + 4 * A_BYTES + FIXED <= BUDGET ? 4 : 2);
@@ -137,12 +141,15 @@ struct Layout {
                           : (BUDGET - FIXED - BS_PREF * B_BYTES) / A_BYTES;
   static constexpr int AS = AS_RAW > 12 ? 12 : AS_RAW;
   static constexpr int BS = (KIND == KIND_F8F8) ? AS : BS_PREF;
-  static constexpr int TOTAL = AS * A_BYTES + CS * C_BYTES + BS * B_BYTES + OUT_BYTES + MISC_BYTES;
-  static constexpr int NBUF = BT > 128 ? 2 : 4;            // TMEM accumulator buffers
+  static constexpr int TOTAL = AS * A_BYTES + BS * B_BYTES + OUT_BYTES + MISC_BYTES;
+  // TMEM accumulator buffers (the bf16 kinds keep columns 256.. for the
+  // decoded-weight ring)
+  static constexpr int NBUF = (BT > 128 || (KIND != KIND_F8F8 && BT == 128)) ? 2 : 4;
   // each accumulator starts at a power-of-two column offset (192-wide tiles
   // take 256-column slots); the allocation is a power of two
   static constexpr int BSTRIDE = BT > 128 ? 256 : BT;
-  static constexpr int TMEM_COLS = NBUF * BSTRIDE;
+  static constexpr int TMEM_COLS = (KIND == KIND_F8F8) ? NBUF * BSTRIDE : 512;
+  static_assert(KIND == KIND_F8F8 || NBUF * BSTRIDE <= C_TCOL, "accumulators overlap the decode ring");
   static_assert(AS >= 2 && BS >= 2, "pipeline too shallow");
   static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory over budget");
   static_assert(COLS % 32 == 0 && COLS <= 128, "epilogue column split");
@@ -302,8 +309,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   // turn every shared access below into a generic one)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;
-  uint8_t* sC = sA + AS * L::A_BYTES;
-  uint8_t* sB = sC + CS * L::C_BYTES;
+  uint8_t* sB = sA + AS * L::A_BYTES;
   float* sOut = reinterpret_cast<float*>(sB + BS * L::B_BYTES);
   uint8_t* misc = reinterpret_cast<uint8_t*>(sOut) + L::OUT_BYTES;
   uint64_t* a_full = reinterpret_cast<uint64_t*>(misc);
@@ -311,8 +317,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   uint64_t* b_full = a_empty + 12;
   uint64_t* b_empty = b_full + 12;
   uint64_t* c_full = b_empty + 12;
-  uint64_t* c_empty = c_full + 2;
-  uint64_t* t_full = c_empty + 2;
+  uint64_t* c_empty = c_full + 4;
+  uint64_t* t_full = c_empty + 4;
   uint64_t* t_empty = t_full + 4;
   uint64_t* s_full = t_empty + 4;
   uint64_t* s_empty = s_full + SSL;
@@ -458,14 +464,15 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
             }
             mma_commit(&a_empty[sa]);
           } else {
-            const uint32_t a0 = smem_u32(sC + sa * L::C_BYTES);
+            // A = the decoded slice in TMEM (row = lane, two bf16 per column:
+            // K-step j of 16 reads columns 8j .. 8j+7), B = tokens in shared
+            const uint32_t a0 = tmem_base + L::C_TCOL + sa * 64;
             const uint32_t b0 = smem_u32(sB + sb * L::B_BYTES);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const uint32_t acc = PROMOTE ? (j > 0) : (!first || j > 0);
-              const uint32_t ao = a0 + (j >> 2) * 16384 + (j & 3) * 32;
               const uint32_t bo = b0 + (j >> 2) * (brows * 128) + (j & 3) * 32;
-              mma_f16(d, sw128_desc(ao), sw128_desc(bo), idesc, acc);
+              mma_f16_ts(d, a0 + 8 * j, sw128_desc(bo), idesc, acc);
             }
             mma_commit(&c_empty[sa]);
           }
@@ -680,11 +687,16 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     }
   } else if (warp >= L::CONV_WARP0) {
     // ------------------------------------------- weight decode to bf16
-    // 8 warps; every thread loads all of its source chunks of the slice
-    // before converting, so the shared-memory latency overlaps.
+    // Thread = weight row of the tile = TMEM lane; the two warps of a lane
+    // quarter take the two 64-wide K halves of the slice.  Each thread reads
+    // its row's bytes from the (swizzled) shared tile, decodes them and
+    // stores 32 columns of bf16 pairs into the TMEM ring slot, which the
+    // MMA then reads as its A operand.
     if constexpr (KIND != KIND_F8F8) {
-      constexpr int CT = 32 * L::NCV;
-      const int ct = threadIdx.x - 32 * L::CONV_WARP0;
+      const int half = (warp - L::CONV_WARP0) >> 2;
+      const int r = (warp & 3) * 32 + lane;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
+                             L::C_TCOL + half * 32;
       uint32_t ia = 0, ic = 0, is = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
@@ -692,58 +704,51 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           const int sa = ia % AS, sc = ic % CS;
           if (!mbar_wait(&a_full[sa], (ia / AS) & 1, wc)) goto conv_done;
           if (!mbar_wait(&c_empty[sc], ((ic / CS) & 1) ^ 1, wc)) goto conv_done;
+          tc_fence_after();
           const uint8_t* src = sA + sa * L::A_BYTES;
-          uint8_t* dst = sC + sc * L::C_BYTES;
+          uint32_t w[32];
           if (KIND == KIND_F8W) {
-            // 1024 chunks of 16 fp8 (row r, chunk c); swizzled source rows
-            constexpr int PER = 1024 / CT;
-            uint4 raw[PER];
+            // 64 fp8 of row r: 16-byte chunks 4*half .. 4*half+3 of the
+            // 128-byte row, stored with the 128-byte swizzle
+            uint4 raw[4];
 #pragma unroll
-            for (int i = 0; i < PER; ++i) {
-              const int q = i * CT + ct;
-              const int r = q >> 3, c = q & 7;
+            for (int i = 0; i < 4; ++i) {
+              const int c = 4 * half + i;
               raw[i] = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_empty[sa]);
 #pragma unroll
-            for (int i = 0; i < PER; ++i) {
-              const int q = i * CT + ct;
-              const int r = q >> 3, c = q & 7;
-              uint4 o0, o1;
-              o0.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].x));
-              o0.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].x >> 16));
-              o0.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].y));
-              o0.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].y >> 16));
-              o1.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].z));
-              o1.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].z >> 16));
-              o1.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].w));
-              o1.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(raw[i].w >> 16));
-              const int h = c >> 2, cc = (c & 3) * 2;
-              uint8_t* rowp = dst + h * 16384 + r * 128;
-              *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = o0;
-              *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ (r & 7)) << 4)) = o1;
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t in[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                w[8 * i + 2 * t] = e4m3x2_to_bf16x2(static_cast<uint16_t>(in[t]));
+                w[8 * i + 2 * t + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(in[t] >> 16));
+              }
             }
           } else {
-            // 512 chunks of 32 e2m1 (row r, 32-element group c), linear source;
-            // the group's ue8m0 byte comes from the shared scale ring
-            constexpr int PER = 512 / CT;
+            // 64 e2m1 of row r: 16-byte chunks 2*half, 2*half+1 of the
+            // 64-byte row (64-byte swizzle); chunk c is the 32-group with
+            // ue8m0 scale byte c of the slice
             const int slot = is % SSL;
             if (!mbar_wait(&s_full[slot], (is / SSL) & 1, wc)) goto conv_done;
-            uint4 raw[PER];
-            uint32_t ev[PER];
+            const uint32_t e4 = sMx[slot * 128 + r];
+            uint4 raw[2];
 #pragma unroll
-            for (int i = 0; i < PER; ++i) {
-              const int q = i * CT + ct;
-              raw[i] = *reinterpret_cast<const uint4*>(src + q * 16);
-              ev[i] = (sMx[slot * 128 + (q >> 2)] >> (8 * (q & 3))) & 0xFFu;
+            for (int k = 0; k < 2; ++k) {
+              const int c = 2 * half + k;
+              raw[k] = *reinterpret_cast<const uint4*>(src + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[slot]);
+            if (lane == 0) {
+              mbar_arrive(&a_empty[sa]);
+              mbar_arrive(&s_empty[slot]);
+            }
             ++is;
 #pragma unroll
-            for (int i = 0; i < PER; ++i) {
-              const int q = i * CT + ct;
-              const int r = q >> 2, c = q & 3;
-              const uint32_t e = ev[i];
+            for (int k = 0; k < 2; ++k) {
+              const uint32_t e = (e4 >> (8 * (2 * half + k))) & 0xFFu;
               // bf16 2^(e - 127 + 112) when representable; else two steps
               __nv_bfloat162 sc2;
               uint32_t two_step = 0;
@@ -758,43 +763,30 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
                   sc2 = *reinterpret_cast<const __nv_bfloat162*>(&bits);
                 }
               }
-              uint32_t w[16];
-              const uint32_t in[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+              const uint32_t in[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
 #pragma unroll
                 for (int bb = 0; bb < 4; ++bb)
-                  w[j * 4 + bb] = e2m1x2_to_bf16x2((in[j] >> (8 * bb)) & 0xFFu, sc2);
+                  w[16 * k + 4 * j + bb] = e2m1x2_to_bf16x2((in[j] >> (8 * bb)) & 0xFFu, sc2);
               }
               if (two_step) {
                 const float f = ldexpf(1.0f, static_cast<int>(e) - 127);
                 const __nv_bfloat162 s2 = __floats2bfloat162_rn(f, f);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w[j]);
+                  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w[16 * k + j]);
                   v = __hmul2(v, s2);
-                  w[j] = *reinterpret_cast<uint32_t*>(&v);
+                  w[16 * k + j] = *reinterpret_cast<uint32_t*>(&v);
                 }
-              }
-              const int h = c >> 1, cc0 = (c & 1) * 4;
-              uint8_t* rowp = dst + h * 16384 + r * 128;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint4 o;
-                o.x = w[j * 4 + 0];
-                o.y = w[j * 4 + 1];
-                o.z = w[j * 4 + 2];
-                o.w = w[j * 4 + 3];
-                *reinterpret_cast<uint4*>(rowp + (((cc0 + j) ^ (r & 7)) << 4)) = o;
               }
             }
           }
-          fence_proxy_async_smem();
+          tmem_st32(t_row + sc * 64, w);
+          tmem_st_wait();
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&c_full[sc]);
-            mbar_arrive(&a_empty[sa]);
-          }
+          if (lane == 0) mbar_arrive(&c_full[sc]);
         }
       }
     conv_done:;
