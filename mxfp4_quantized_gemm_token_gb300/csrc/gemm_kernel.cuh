@@ -415,32 +415,48 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         for (uint32_t i = first; i < it; ++i) mbar_wait(&a_full[i % AS], (i / AS) & 1, dw);
       }
     }
-  } else if (warp == 1 || (PROMOTE && warp == 2)) {
+  } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------ MMA issuer
     // the whole warp runs the loop; one elected lane issues.  With per-slice
     // promotion every slice has its own TMEM buffer and two issuing warps
     // take every other slice.
     {
-      constexpr uint32_t NISS = PROMOTE ? 2 : 1;
-      const uint32_t mine = static_cast<uint32_t>(warp - 1);
+      // Two issuers.  Promoted kinds: every slice has its own buffer and
+      // the issuers take alternate slices.  Whole-K kinds: each unit has a
+      // pair of accumulators, issuer i summing the unit's slices l with
+      // l % 2 == i into buffer (2 * unit + i) % NB; the epilogue adds the
+      // pair.  An issuer with no slice in a unit (one-slice units) hands
+      // over its buffer unwritten, so every barrier phase stays in step.
+      constexpr uint32_t NISS = 2;
+      const uint32_t mine = (warp == 1) ? 0u : 1u;
       uint32_t ia = 0, ib = 0, au = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
         const int brows = U.brows;
+        const int nsl = U.kb1 - U.kb0;
         const uint32_t idesc =
             (KIND == KIND_F8F8) ? idesc_e4m3(128, U.n_inst) : idesc_bf16(128, U.n_inst);
+        uint32_t ubuf = 0;
+        if (!PROMOTE) {
+          const uint32_t tb = 2 * au + mine;
+          ubuf = tb % NB;
+          if (!mbar_wait_warp(&t_empty[ubuf], ((tb / NB) & 1) ^ 1, wc)) goto mma_done;
+          if (nsl <= static_cast<int>(mine)) {
+            if (elect_one()) mma_commit(&t_full[ubuf]);
+            __syncwarp();
+          }
+        }
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
-          const bool first = (kb == U.kb0), last = (kb == U.kb1 - 1);
-          if (NISS > 1 && ia % NISS != mine) {
-            // the other issuer's slice (promoted: every slice advances
-            // every counter)
+          const int l = kb - U.kb0;
+          const bool take = PROMOTE ? (ia % NISS == mine) : (static_cast<uint32_t>(l) % NISS == mine);
+          if (!take) {
             ++ia;
             ++ib;
-            ++au;
+            if (PROMOTE) ++au;
             continue;
           }
-          const uint32_t buf = au % NB;
-          if (PROMOTE || first)
+          const uint32_t buf = PROMOTE ? au % NB : ubuf;
+          if (PROMOTE)
             if (!mbar_wait_warp(&t_empty[buf], ((au / NB) & 1) ^ 1, wc)) goto mma_done;
           // FP8 x FP8 reads the A ring; the bf16 kinds read the decoded C ring
           constexpr int RA = (KIND == KIND_F8F8) ? AS : CS;
@@ -452,6 +468,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
             if (!mbar_wait_warp(&b_full[sb], (ib / BS) & 1, wc)) goto mma_done;
           tc_fence_after();
           const uint32_t d = tmem_base + buf * L::BSTRIDE;
+          // accumulate except on the first K step of this issuer's first slice
+          const bool fresh = PROMOTE || static_cast<uint32_t>(l) == mine;
           const bool leader = elect_one();
           if (leader) {
           if (KIND == KIND_F8F8) {
@@ -459,7 +477,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
             const uint32_t b0 = smem_u32(sB + sb * L::B_BYTES);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const uint32_t acc = PROMOTE ? (j > 0) : (!first || j > 0);
+              const uint32_t acc = (fresh && j == 0) ? 0u : 1u;
               mma_f8f6f4(d, sw128_desc(a0 + 32 * j), sw128_desc(b0 + 32 * j), idesc, acc);
             }
             mma_commit(&a_empty[sa]);
@@ -470,7 +488,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
             const uint32_t b0 = smem_u32(sB + sb * L::B_BYTES);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const uint32_t acc = PROMOTE ? (j > 0) : (!first || j > 0);
+              const uint32_t acc = (fresh && j == 0) ? 0u : 1u;
               const uint32_t bo = b0 + (j >> 2) * (brows * 128) + (j & 3) * 32;
               mma_f16_ts(d, a0 + 8 * j, sw128_desc(bo), idesc, acc);
             }
@@ -480,11 +498,15 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           }
           ++ia;
           ++ib;
-          if (PROMOTE || last) {
+          if (PROMOTE) {
             if (leader) mma_commit(&t_full[buf]);
             ++au;
+          } else if (l + static_cast<int>(NISS) >= nsl) {
+            if (leader) mma_commit(&t_full[buf]);   // this issuer's last slice of the unit
           }
+          __syncwarp();
         }
+        if (!PROMOTE) ++au;
       }
     mma_done:
       if (*abort_flag) {
@@ -978,16 +1000,32 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         }
       } else {
         if (p.block_n == 0 && p.w_scale != nullptr) fscale = __ldg(p.w_scale);
-        const uint32_t buf = au % NB;
-        if (!mbar_wait(&t_full[buf], (au / NB) & 1, wc)) goto epi_done;
+        // the unit's two accumulators (one per MMA issuer); the second is
+        // unwritten when the unit has a single K slice
+        const uint32_t tb0 = 2 * au, tb1 = 2 * au + 1;
+        const uint32_t buf0 = tb0 % NB, buf1 = tb1 % NB;
+        const bool two = U.kb1 - U.kb0 >= 2;
+        if (!mbar_wait(&t_full[buf0], (tb0 / NB) & 1, wc)) goto epi_done;
+        if (!mbar_wait(&t_full[buf1], (tb1 / NB) & 1, wc)) goto epi_done;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < COLS / GRP; ++c) {
-          if (c < ngr) tmem_ld<GRP>(tmem_base + lane_addr + buf * L::BSTRIDE + col0 + c * GRP, &acc[c * GRP]);
+          if (c < ngr) {
+            tmem_ld<GRP>(tmem_base + lane_addr + buf0 * L::BSTRIDE + col0 + c * GRP, &acc[c * GRP]);
+            if (two) {
+              float v[GRP];
+              tmem_ld<GRP>(tmem_base + lane_addr + buf1 * L::BSTRIDE + col0 + c * GRP, v);
+#pragma unroll
+              for (int j = 0; j < GRP; ++j) acc[c * GRP + j] += v[j];
+            }
+          }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&t_empty[buf]);
+        if (lane == 0) {
+          mbar_arrive(&t_empty[buf0]);
+          mbar_arrive(&t_empty[buf1]);
+        }
         ++au;
       }
       // ------------------------------------------------------- output

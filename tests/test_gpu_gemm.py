@@ -108,6 +108,25 @@ def test_w8a16_per_tensor_config(oracle):
     assert_bf16_close(o16, rb)
 
 
+@pytest.mark.parametrize("K,split", [(64, 0), (128, 0), (192, 0), (256, 0), (384, 3), (640, 2)])
+def test_w8a16_per_tensor_short_k_and_split(oracle, K, split):
+    """Whole-K accumulation over one or two 128-wide slices (the two MMA
+    issuers then hold one slice each, or one holds none), and split-K units of
+    a single slice."""
+    a, w, scale, bias = synth.per_tensor_fp8_problem(M=33, N=256, K=K, seed=K)
+    rf, rb = oracle.scaled_mm(bits16(a), BF16, None, u8(w), scale.numpy(), 0, 0, bias.numpy())
+    try:
+        mxq.set_option(_lib.OPT_SPLIT_K, split)
+        o32 = mxq.fp8_scaled_mm(a.cuda(), w.cuda(), scale.cuda(), None, bias=bias.cuda(),
+                                out_dtype=torch.float32)
+        o16 = mxq.fp8_scaled_mm(a.cuda(), w.cuda(), scale.cuda(), None, bias=bias.cuda())
+        mxq.sync_status()
+    finally:
+        mxq.set_option(_lib.OPT_SPLIT_K, 0)
+    assert_probe_close(o32, rf)
+    assert_bf16_close(o16, rb)
+
+
 def test_per_tensor_equals_constant_blocks_on_gpu():
     a, w, scale, bias = synth.per_tensor_fp8_problem(M=40, N=256, K=512, seed=3)
     ac, wc = a.cuda(), w.cuda()

@@ -106,6 +106,16 @@ def test_fused_mxfp4_bias(oracle, block_m):
     run_moe(oracle, W_MX, E, N, K, x, tw, ids, block_m, bias=True)
 
 
+@pytest.mark.parametrize("wtype", [W_FP8, W_MX])
+def test_fused_single_slice_stages(oracle, wtype):
+    """K = 128 and N = 64: both GEMM stages reduce over one 128-wide slice,
+    so one of the two MMA issuers has no slice in any unit."""
+    E, N, K, T, topk = 4, 64, 128, 11, 2
+    x = synth.activations(T, K, seed=13, scale_div=10)
+    tw, ids = synth.routing_uniform(T, E, topk, seed=14)
+    run_moe(oracle, wtype, E, N, K, x, tw, ids, 16, bias=(wtype == W_MX))
+
+
 @pytest.mark.parametrize("topk", [1, 8])
 def test_fused_small_expert_blocks_4_5_33(oracle, topk):
     """Expert blocks of exactly 0, 4, 5 and 33 tokens (the vLLM CPU page's
