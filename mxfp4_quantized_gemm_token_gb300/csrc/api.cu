@@ -225,7 +225,7 @@ MmPlan plan_mm(int64_t M, int64_t N, int64_t K, int32_t a_dtype, bool block, boo
     // clear of spills (512 threads); 256 packs fewer waves when the token
     // count is small
     pl.bt = nt > 0 ? static_cast<int>(nt)
-                   : (N < 4096 ? 128 : (M >= 2048 ? 192 : (M >= 512 ? 256 : 128)));
+                   : (N < 4096 ? 128 : (M >= 1024 ? 192 : (M >= 512 ? 256 : 128)));
   }
   pl.promote = block || has_ascale;
   pl.tiles_n = static_cast<int>(cdiv(N, pl.normal ? pl.bt : 128));
