@@ -355,6 +355,58 @@ def _timed_calls(fn, reps, flush):
     return statistics.median(ts)
 
 
+def _graph_timed_calls(fn, reps, flush):
+    """Median device time (ms) of one CUDA-graph replay of fn() (captured
+    once after warm-up), L2 flushed before each replay; None if fn cannot be
+    captured."""
+    try:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+    except Exception as e:  # capture not possible: report eager only
+        print(json.dumps({"graph_capture_error": str(e)[:200]}), file=sys.stderr)
+        return None
+    return _timed_calls(g.replay, reps, flush)
+
+
+def run_fp8_peak(local):
+    """Burst dense FP8 (e4m3 x e4m3 -> bf16) rate of the vendor library GEMM,
+    torch._scaled_mm at 8192^3, best of 10 CUDA-event timings; reported next
+    to the roofline denominator (2 x the measured bf16 burst), not used as it."""
+    dev = torch.device("cuda", local)
+    n = 8192
+    g = torch.Generator(device=dev).manual_seed(0)
+    a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+    one = torch.tensor(1.0, device=dev)
+    f = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+    for _ in range(3):
+        f()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        f()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    pk, src = peaks()
+    tf = 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    print(json.dumps({"fp8_burst_tflops_vendor_gemm": tf, "shape": [n, n, n], "best_ms": best,
+                      "bf16_x2_denominator": 2.0 * pk["bf16_tflops"], "bf16_source": src}),
+          flush=True)
+    return 0
+
+
 def run_workloads(args, local):
     """One JSON line per shape of the other hot-path configurations (for the
     results tables): per-tensor W8A16, [1,128] block W8A8, fused MoE FP8-block
@@ -379,9 +431,12 @@ def run_workloads(args, local):
             a, w, scale, bias = a.to(dev), w.to(dev), scale.to(dev), bias.to(dev)
             for _ in range(args.warmup):
                 mxq.fp8_per_tensor_linear(a, w, scale, bias)
-            ms = _timed_calls(lambda: mxq.fp8_per_tensor_linear(a, w, scale, bias), reps, flush)
+            f = lambda: mxq.fp8_per_tensor_linear(a, w, scale, bias)
+            ms = _timed_calls(f, reps, flush)
+            gms = _graph_timed_calls(f, reps, flush)
             byts = 97 * 576 * 2 + 224 * 576 + 224 * 4 + 97 * 224 * 2
             emit({"M": 97, "N": 224, "K": 576, "us": ms * 1e3,
+                  "us_graph": None if gms is None else gms * 1e3,
                   "TFLOPs": 2 * 97 * 224 * 576 / ms / 1e9, "GBs": byts / ms / 1e6})
         elif name == "block1x128":
             w, ws = synth.block_fp8_weight(4096, 7168, 1, seed=1, device=dev)
@@ -395,8 +450,10 @@ def run_workloads(args, local):
                 for _ in range(args.warmup):
                     f()
                 ms = _timed_calls(f, reps, flush)
+                gms = _graph_timed_calls(f, reps, flush)
                 byts = 4096 * 7168 + 4096 * 56 * 4 + M * 7168 * 2 + M * 4096 * 2
                 emit({"M": M, "N": 4096, "K": 7168, "us": ms * 1e3,
+                      "us_graph": None if gms is None else gms * 1e3,
                       "TFLOPs": 2 * M * 4096 * 7168 / ms / 1e9, "GBs": byts / ms / 1e6,
                       "hbm_frac": byts / ms / 1e6 / hbm})
         elif name in ("moe_fp8", "moe_mxfp4"):
@@ -433,10 +490,11 @@ def run_workloads(args, local):
                         f()
                     mxq.sync_status(dev)
                     ms = _timed_calls(f, reps, flush)
+                    gms = _graph_timed_calls(f, reps, flush)
                     byts = touched * per_expert + T * K * 4
                     flops = T * topk * (2 * K * 2 * N + 2 * N * K)
                     emit({"T": T, "routing": routing, "experts_touched": touched, "block_m": bm,
-                          "us": ms * 1e3, "TFLOPs": flops / ms / 1e9, "GBs": byts / ms / 1e6,
+                          "us": ms * 1e3, "us_graph": None if gms is None else gms * 1e3, "TFLOPs": flops / ms / 1e9, "GBs": byts / ms / 1e6,
                           "hbm_frac": byts / ms / 1e6 / hbm})
     return 0
 
@@ -448,6 +506,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mxq", choices=["mxq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8-peak", action="store_true",
+                    help="measure the vendor FP8 GEMM burst rate (8192^3) and exit")
     ap.add_argument("--workload", default="",
                     help="comma list of pertensor, block1x128, moe_fp8, moe_mxfp4 (tables only)")
     ap.add_argument("--block-m", type=int, default=64)
@@ -463,6 +523,8 @@ def main():
         return run_reference(args, world, rank)
     if args.profile:
         return run_profile(args, local)
+    if args.fp8_peak:
+        return run_fp8_peak(local)
     if args.workload:
         return run_workloads(args, local)
     return run_gpu(args, world, rank, local)

@@ -259,32 +259,36 @@ __device__ __forceinline__ float load_bias(const GemmParams& p, int64_t idx) {
 }
 
 // ------------------------------------------------------------ weight decode
-// e4m3 pair -> bf16 pair, exactly: the pair is first widened to f16 (every
-// e4m3 value is a normal f16 or zero), whose bits shifted right by 3 form a
-// bf16 with the same mantissa and a biased exponent 112 short; one bf16
-// multiply by 2^112 restores it (zero stays zero).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
-  uint32_t h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
+// Weight decode, exact.  Every e4m3 value and every e2m1 value is a normal f16
+// (or zero), so the pair is first widened to f16; those bits shifted right by
+// 3 form a bf16 with the same mantissa and a biased exponent 112 short, and
+// one bf16 multiply by 2^112 (or, for MXFP4, by 2^(e - 127 + 112), the
+// group's ue8m0 scale folded in) restores the value.  The 32-bit source word
+// is split into byte / half registers by a vector move, so no extraction
+// instructions are spent (the decode is bound by the integer ALU pipe).
+__device__ __forceinline__ uint32_t f16x2_bits_to_bf16x2(uint32_t h, uint32_t k2) {
   uint32_t t = ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
   __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&t);
-  const uint32_t k2 = 0x77807780u;   // bf16 pair (2^112, 2^112)
   v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&k2));
   return *reinterpret_cast<uint32_t*>(&v);
 }
-
-// e2m1 pair (one byte, low nibble first) -> bf16 pair times the block scale
-// pair `sc` (already including 2^112, see above).
-__device__ __forceinline__ uint32_t e2m1x2_to_bf16x2(uint32_t byte, __nv_bfloat162 sc) {
-  uint32_t h;
-  asm("{ .reg .b8 t; .reg .b16 s; cvt.u16.u32 s, %1; cvt.u8.u16 t, s;"
-      " cvt.rn.f16x2.e2m1x2 %0, t; }"
-      : "=r"(h)
-      : "r"(byte));
-  uint32_t t = ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
-  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&t);
-  v = __hmul2(v, sc);
-  return *reinterpret_cast<uint32_t*>(&v);
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t word, uint32_t& lo, uint32_t& hi) {
+  uint32_t h0, h1;
+  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.rn.f16x2.e4m3x2 %0, a; cvt.rn.f16x2.e4m3x2 %1, b; }"
+      : "=r"(h0), "=r"(h1) : "r"(word));
+  lo = f16x2_bits_to_bf16x2(h0, 0x77807780u);
+  hi = f16x2_bits_to_bf16x2(h1, 0x77807780u);
+}
+__device__ __forceinline__ void e2m1x8_to_bf16x8(uint32_t word, uint32_t k2, uint32_t* o) {
+  uint32_t h0, h1, h2, h3;
+  asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;"
+      " cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;"
+      " cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3) : "r"(word));
+  o[0] = f16x2_bits_to_bf16x2(h0, k2);
+  o[1] = f16x2_bits_to_bf16x2(h1, k2);
+  o[2] = f16x2_bits_to_bf16x2(h2, k2);
+  o[3] = f16x2_bits_to_bf16x2(h3, k2);
 }
 
 // Barrier of the 128 epilogue threads on an mbarrier, so that it is bounded
@@ -745,8 +749,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
               const uint32_t in[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
               for (int t = 0; t < 4; ++t) {
-                w[8 * i + 2 * t] = e4m3x2_to_bf16x2(static_cast<uint16_t>(in[t]));
-                w[8 * i + 2 * t + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(in[t] >> 16));
+                e4m3x4_to_bf16x4(in[t], w[8 * i + 2 * t], w[8 * i + 2 * t + 1]);
               }
             }
           } else {
@@ -787,11 +790,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
               }
               const uint32_t in[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-#pragma unroll
-                for (int bb = 0; bb < 4; ++bb)
-                  w[16 * k + 4 * j + bb] = e2m1x2_to_bf16x2((in[j] >> (8 * bb)) & 0xFFu, sc2);
-              }
+              for (int j = 0; j < 4; ++j)
+                e2m1x8_to_bf16x8(in[j], *reinterpret_cast<const uint32_t*>(&sc2), &w[16 * k + 4 * j]);
               if (two_step) {
                 const float f = ldexpf(1.0f, static_cast<int>(e) - 127);
                 const __nv_bfloat162 s2 = __floats2bfloat162_rn(f, f);

@@ -9,7 +9,8 @@
 //
 // Memory-bound: 2 bytes in, 1 + 4/128 bytes out per element.  The fast path
 // gives each 128-element group to a half warp (8 contiguous bf16 = one 16-byte
-// load per lane), reduces amax with shuffles, and writes 8 codes per lane.
+// load per lane), reduces amax with shuffles, and writes 8 codes per lane;
+// each half warp handles four groups at a time to keep loads in flight.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -30,56 +31,68 @@ __device__ __forceinline__ uint16_t e4m3x2_rn(float lo, float hi) {
   return r;
 }
 
-// group == 128, K % 128 == 0, 16-byte aligned rows
+// group == 128, K % 128 == 0, 16-byte aligned rows.  A warp takes 8 groups
+// per iteration (each half warp 4): all 4 loads of a lane are issued before
+// any of them is used, so 64 bytes per lane are in flight.
 __global__ void group_quant128_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K,
                                       int64_t ldx, float eps, uint8_t* __restrict__ q,
                                       float* __restrict__ scales) {
+  constexpr int U = 4;
   const int64_t G = K / 128;
   const int64_t total = M * G;
   const int lane = threadIdx.x & 31;
   const int hl = lane & 15;
+  const int hw = lane >> 4;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       2 * w < total; w += nwarps) {
-    const int64_t item = 2 * w + (lane >> 4);
-    const bool valid = item < total;
-    const int64_t m = valid ? item / G : 0;
-    const int64_t g = valid ? item - m * G : 0;
-    float v[8];
-    float amax = 0.f;
-    if (valid) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(x + m * ldx + g * 128 + hl * 8));
-      const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+       2 * U * w < total; w += nwarps) {
+    uint4 raw[U];
+    int64_t mm[U], gg[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t item = 2 * U * w + 2 * u + hw;
+      ok[u] = item < total;
+      mm[u] = ok[u] ? item / G : 0;
+      gg[u] = ok[u] ? item - mm[u] * G : 0;
+      raw[u] = ok[u] ? __ldg(reinterpret_cast<const uint4*>(x + mm[u] * ldx + gg[u] * 128 + hl * 8))
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float v[8];
+      const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         v[2 * i] = __uint_as_float(wv[i] << 16);
         v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
       }
+      float amax = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float a = fabsf(v[i]);
         amax = (a > amax) ? a : amax;
       }
-    }
 #pragma unroll
-    for (int off = 8; off >= 1; off >>= 1) {
-      const float o = __shfl_xor_sync(0xffffffffu, amax, off);
-      amax = (o > amax) ? o : amax;
-    }
-    if (valid) {
-      const float s = __fdiv_rn((amax > eps) ? amax : eps, 448.f);
-      uint32_t pk[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float* vv = v + 4 * h;
-        const uint16_t a =
-            e4m3x2_rn(clamp448(__fdiv_rn(vv[0], s)), clamp448(__fdiv_rn(vv[1], s)));
-        const uint16_t b =
-            e4m3x2_rn(clamp448(__fdiv_rn(vv[2], s)), clamp448(__fdiv_rn(vv[3], s)));
-        pk[h] = static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
+      for (int off = 8; off >= 1; off >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, amax, off);
+        amax = (o > amax) ? o : amax;
       }
-      *reinterpret_cast<uint2*>(q + m * K + g * 128 + hl * 8) = make_uint2(pk[0], pk[1]);
-      if (hl == 0) scales[m * G + g] = s;
+      if (ok[u]) {
+        const float s = __fdiv_rn((amax > eps) ? amax : eps, 448.f);
+        uint32_t pk[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float* vv = v + 4 * h;
+          const uint16_t a =
+              e4m3x2_rn(clamp448(__fdiv_rn(vv[0], s)), clamp448(__fdiv_rn(vv[1], s)));
+          const uint16_t b =
+              e4m3x2_rn(clamp448(__fdiv_rn(vv[2], s)), clamp448(__fdiv_rn(vv[3], s)));
+          pk[h] = static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
+        }
+        *reinterpret_cast<uint2*>(q + mm[u] * K + gg[u] * 128 + hl * 8) = make_uint2(pk[0], pk[1]);
+        if (hl == 0) scales[mm[u] * G + gg[u]] = s;
+      }
     }
   }
 }
@@ -124,9 +137,21 @@ cudaError_t launch_group_quant(const void* x, int64_t M, int64_t K, int64_t ldx,
                     (reinterpret_cast<uintptr_t>(q) & 7) == 0;
   const int threads = 256;
   const int64_t G = (K + group - 1) / group;
-  const int64_t items = fast ? (M * G + 1) / 2 : M * G;       // warps of work
+  const int64_t items = fast ? (M * G + 7) / 8 : M * G;       // warps of work
   int64_t blocks = (items + (threads / 32) - 1) / (threads / 32);
-  const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+  // a persistent grid of the blocks that fit at once (no ragged last wave)
+  static int resident[2] = {0, 0};
+  int& res = resident[fast ? 1 : 0];
+  if (res == 0) {
+    int r = 0;
+    cudaError_t e = fast ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, group_quant128_kernel,
+                                                                       threads, 0)
+                         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                               &r, group_quant_generic_kernel, threads, 0);
+    if (e != cudaSuccess) return e;
+    res = r > 0 ? r : 1;
+  }
+  const int64_t cap = static_cast<int64_t>(num_sms) * res;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (fast)
