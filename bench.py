@@ -355,6 +355,34 @@ def _timed_calls(fn, reps, flush):
     return statistics.median(ts)
 
 
+def run_profile_moe(args, local):
+    """Two fused-MoE calls of one shape, for ncu captures of the MoE kernels:
+    --profile-moe fp8:T:E (FP8-block, topk 8, K 7168, N 2048) or
+    mxfp4:T:E (MXFP4 + bias, topk 4, K = N = 2880); uniform routing."""
+    import mxfp4_quantized_gemm_token_gb300 as mxq
+    from mxfp4_quantized_gemm_token_gb300 import synth
+    dev = torch.device("cuda", local)
+    kind, T, E = args.profile_moe.split(":")
+    T, E = int(T), int(E)
+    if kind == "fp8":
+        topk, K, N = 8, 7168, 2048
+        w1, s1, w2, s2 = synth.moe_fp8_weights(E, N, K, seed=0, device=dev)
+        kw = {}
+    else:
+        topk, K, N = 4, 2880, 2880
+        w1, s1, w2, s2 = synth.moe_mxfp4_weights(E, N, K, seed=0, device=dev)
+        b1, b2 = synth.moe_biases(E, N, K, seed=1, device=dev)
+        kw = dict(wtype=mxq.W_MXFP4, w1_bias=b1, w2_bias=b2)
+    tw, ids = synth.routing_uniform(T, E, topk, seed=T)
+    x = synth.activations(T, K, seed=T, scale_div=10, device=dev)
+    tw, ids = tw.to(dev), ids.to(dev)
+    for _ in range(2):
+        mxq.fused_experts(x, w1, s1, w2, s2, tw, ids, block_m=args.block_m, **kw)
+    mxq.sync_status(dev)
+    print(json.dumps({"profile_moe": args.profile_moe, "experts_touched": synth.distinct_experts(ids)}))
+    return 0
+
+
 def _graph_timed_calls(fn, reps, flush):
     """Median device time (ms) of one CUDA-graph replay of fn() (captured
     once after warm-up), L2 flushed before each replay; None if fn cannot be
@@ -513,6 +541,8 @@ def main():
     ap.add_argument("--block-m", type=int, default=64)
     ap.add_argument("--profile", type=int, default=0,
                     help="run 3 launches of quant + GEMM at this M only (for ncu)")
+    ap.add_argument("--profile-moe", default="",
+                    help="kind:T:E, e.g. mxfp4:64:128 -- two fused-MoE calls (for ncu)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu DRAM bytes per launch of the dominant kernel (if measured)")
     args = ap.parse_args()
@@ -525,6 +555,8 @@ def main():
         return run_profile(args, local)
     if args.fp8_peak:
         return run_fp8_peak(local)
+    if args.profile_moe:
+        return run_profile_moe(args, local)
     if args.workload:
         return run_workloads(args, local)
     return run_gpu(args, world, rank, local)
