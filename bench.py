@@ -527,6 +527,55 @@ def run_workloads(args, local):
     return 0
 
 
+def run_ablation(args, local):
+    """Per-expert-block path choice vs one path for the whole layer (the global
+    crossover, chosen from max(1, S/E)), and both paths forced, on the MoE
+    workloads under uniform and Zipf routing.  Threshold SMALL_M_MAX = 16
+    slots: blocks (or the layer average) at or below it use the narrowest MMA
+    N that covers them, larger ones the full block_m width."""
+    import mxfp4_quantized_gemm_token_gb300 as mxq
+    from mxfp4_quantized_gemm_token_gb300 import synth, _lib
+    dev = torch.device("cuda", local)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    modes = (("per_block", 0), ("global", 3), ("all_narrow", 1), ("all_full", 2))
+    try:
+        mxq.set_option(_lib.OPT_SMALL_M_MAX, 16)
+        for kind in ("fp8", "mxfp4"):
+            fp8 = kind == "fp8"
+            E, topk, K, N = (256, 8, 7168, 2048) if fp8 else (128, 4, 2880, 2880)
+            Ts = (4, 32, 256) if fp8 else (1, 32, 512)
+            if fp8:
+                w1, s1, w2, s2 = synth.moe_fp8_weights(E, N, K, seed=0, device=dev)
+                kw = {}
+            else:
+                w1, s1, w2, s2 = synth.moe_mxfp4_weights(E, N, K, seed=0, device=dev)
+                b1, b2 = synth.moe_biases(E, N, K, seed=1, device=dev)
+                kw = dict(wtype=mxq.W_MXFP4, w1_bias=b1, w2_bias=b2)
+            for T in Ts:
+                for routing in ("uniform", "zipf"):
+                    rf = synth.routing_uniform if routing == "uniform" else synth.routing_zipf
+                    tw, ids = rf(T, E, topk, seed=T)
+                    touched = synth.distinct_experts(ids)
+                    x = synth.activations(T, K, seed=T, scale_div=10, device=dev)
+                    tw, ids = tw.to(dev), ids.to(dev)
+                    line = {"workload": "moe_ablation", "kind": kind, "T": T, "routing": routing,
+                            "experts_touched": touched, "avg_m": max(1, T * topk // E),
+                            "block_m": args.block_m, "small_m_max": 16}
+                    for name, force in modes:
+                        mxq.set_option(_lib.OPT_FORCE_PATH, force)
+                        f = lambda: mxq.fused_experts(x, w1, s1, w2, s2, tw, ids,
+                                                      block_m=args.block_m, **kw)
+                        for _ in range(args.warmup):
+                            f()
+                        mxq.sync_status(dev)
+                        line["us_" + name] = _timed_calls(f, args.steps, flush) * 1e3
+                    print(json.dumps(line), flush=True)
+    finally:
+        mxq.set_option(_lib.OPT_FORCE_PATH, 0)
+        mxq.set_option(_lib.OPT_SMALL_M_MAX, 1 << 30)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -557,6 +606,8 @@ def main():
         return run_fp8_peak(local)
     if args.profile_moe:
         return run_profile_moe(args, local)
+    if args.workload == "moe_ablation":
+        return run_ablation(args, local)
     if args.workload:
         return run_workloads(args, local)
     return run_gpu(args, world, rank, local)

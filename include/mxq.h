@@ -69,7 +69,9 @@ enum {
   MXQ_OPT_SMALL_M_MAX = 1,  /* expert blocks with m_size <= this use the narrowest MMA
                                instruction covering them; larger blocks use the full
                                block_m width.  Default 1 << 30 (always fit). */
-  MXQ_OPT_FORCE_PATH = 2,   /* 0 auto, 1 always narrow (fit), 2 always full width */
+  MXQ_OPT_FORCE_PATH = 2,   /* 0 per expert block (auto), 1 always narrow (fit), 2 always
+                               full width, 3 one path for the whole layer: narrow when
+                               max(1, S / E) <= SMALL_M_MAX (the global crossover) */
   MXQ_OPT_WAIT_BUDGET_NS = 3, /* limit of every device-side wait, default 2e9 ns */
   MXQ_OPT_SPLIT_K = 4,      /* fp8_scaled_mm split-K: 0 auto, else the factor */
   MXQ_OPT_INJECT_STALL = 5, /* TEST ONLY: GEMM producers issue no copy, so every

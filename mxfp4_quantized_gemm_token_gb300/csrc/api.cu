@@ -140,8 +140,9 @@ extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
       value != 256)
     return fail(MXQ_ERR_INVALID_ARG, "TILE_N is 0 (auto), 32, 64, 128 or 256");
   if (value < 0) return fail(MXQ_ERR_INVALID_ARG, "option values are non-negative");
-  if (opt == MXQ_OPT_FORCE_PATH && value > 2)
-    return fail(MXQ_ERR_INVALID_ARG, "FORCE_PATH is 0 (auto), 1 (narrow) or 2 (full width)");
+  if (opt == MXQ_OPT_FORCE_PATH && value > 3)
+    return fail(MXQ_ERR_INVALID_ARG,
+                "FORCE_PATH is 0 (per block), 1 (narrow), 2 (full width) or 3 (one path per layer)");
   g_opts[opt].store(value);
   return MXQ_OK;
 }
@@ -510,11 +511,17 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
   const int kind = fp8 ? KIND_F8W : KIND_MXW;
   const int bt = std::max(32, static_cast<int>(block_m));
   const int64_t force = option(MXQ_OPT_FORCE_PATH);
-  const int narrow_max =
-      force == 2 ? 0
-                 : (force == 1 ? (1 << 30)
-                               : static_cast<int>(std::min<int64_t>(option(MXQ_OPT_SMALL_M_MAX),
-                                                                    1 << 30)));
+  const int64_t small_m = std::min<int64_t>(option(MXQ_OPT_SMALL_M_MAX), 1 << 30);
+  int narrow_max = static_cast<int>(small_m);          // per expert block (the default)
+  if (force == 1) narrow_max = 1 << 30;
+  if (force == 2) narrow_max = 0;
+  if (force == 3) {
+    // one path for the whole layer, chosen from the average slots per
+    // expert, max(1, S / E) (the global crossover the per-block choice is
+    // measured against)
+    const int64_t avg_m = std::max<int64_t>(1, w.S / E);
+    narrow_max = avg_m <= small_m ? (1 << 30) : 0;
+  }
 
   for (int stage = 0; stage < 2; ++stage) {
     // stage 0: act = silu-mul(xs . W1^T);  stage 1: y = w * (act . W2^T + b2)

@@ -48,8 +48,12 @@ def test_version_and_options_roundtrip(lib):
     assert lib.mxq_get_option(_lib.OPT_WAIT_BUDGET_NS, ctypes.byref(v)) == 0 and v.value == 12345
     assert lib.mxq_set_option(_lib.OPT_WAIT_BUDGET_NS, old) == 0
     assert lib.mxq_set_option(99, 1) == _lib.ERR_INVALID_ARG
-    assert lib.mxq_set_option(_lib.OPT_FORCE_PATH, 3) == _lib.ERR_INVALID_ARG
+    assert lib.mxq_set_option(_lib.OPT_FORCE_PATH, 4) == _lib.ERR_INVALID_ARG
     assert b"FORCE_PATH" in lib.mxq_last_error()
+    assert lib.mxq_set_option(_lib.OPT_FORCE_PATH, 3) == 0       # one path per layer
+    assert lib.mxq_set_option(_lib.OPT_FORCE_PATH, 0) == 0
+    assert lib.mxq_set_option(_lib.OPT_NORMAL_TILE, 160) == _lib.ERR_INVALID_ARG
+    assert b"NORMAL_TILE" in lib.mxq_last_error()
 
 
 FAKE = ctypes.c_void_p(1 << 20)   # never dereferenced: validation fails first

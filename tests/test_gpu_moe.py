@@ -129,13 +129,17 @@ def test_fused_small_expert_blocks_4_5_33(oracle, topk):
 
 
 def test_fused_narrow_and_wide_paths_agree(oracle):
+    """Per-block choice (threshold 4), always narrow, always full width and one
+    path for the whole layer all give the oracle's result."""
     E, N, K, T, topk = 8, 128, 256, 21, 2
     x = synth.activations(T, K, seed=11, scale_div=10)
     tw, ids = synth.routing_zipf(T, E, topk, seed=12)
     try:
-        for force in (1, 2):
+        mxq.set_option(_lib.OPT_SMALL_M_MAX, 4)
+        for force in (0, 1, 2, 3):
             mxq.set_option(_lib.OPT_FORCE_PATH, force)
             run_moe(oracle, W_FP8, E, N, K, x, tw, ids, 64)
             run_moe(oracle, W_MX, E, N, K, x, tw, ids, 64)
     finally:
         mxq.set_option(_lib.OPT_FORCE_PATH, 0)
+        mxq.set_option(_lib.OPT_SMALL_M_MAX, 1 << 30)
