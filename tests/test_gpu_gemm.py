@@ -239,6 +239,15 @@ def test_token_major_tile_widths(oracle, tile):
         mxq.set_option(_lib.OPT_NORMAL_TILE, 0)
 
 
+@pytest.mark.parametrize("seed", [71, 72])
+def test_per_row_weight_scales_large_m(oracle, seed):
+    """[1,128] weight scales at M > 512 with ragged token and weight tails and
+    a bias (weight-major tiles, per-row scale per TMEM lane)."""
+    block_case(oracle, 530, 448, 640, 1, seed=seed)
+    block_case(oracle, 600, 200, 384, 1, seed=seed + 10,
+               bias=torch.randn(200, generator=torch.Generator().manual_seed(seed)))
+
+
 @pytest.mark.parametrize("tile", [32, 64, 128, 256])
 def test_forced_token_tile_widths(oracle, tile):
     """Every token-tile width (MMA N and epilogue split) on a ragged shape."""
