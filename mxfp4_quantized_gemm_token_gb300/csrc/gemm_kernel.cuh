@@ -1,35 +1,37 @@
 // gemm_kernel.cuh — the tcgen05 scaled-GEMM kernel behind fp8_scaled_mm and
 // both fused-MoE stages.
 //
-// Orientation ("swap-AB"): the weight matrix W [rows, K] is the MMA's M side
-// (128 rows per tile, one TMEM lane per weight row) and the tokens [tokens, K]
-// are the MMA's N side (BT columns).  Decode-size token counts then cost a
-// narrow instruction instead of a mostly-empty 128-row tile, and the same
-// code serves large token counts with BT = 128.
+// Two orientations.  Weight-major ("swap-AB", EPI_DENSE / SILU / SCATTER):
+// the weight matrix W [rows, K] is the MMA's M side (128 rows per tile, one
+// TMEM lane per weight row) and the tokens are the N side (16 - 128 columns),
+// so decode-size token counts cost a narrow instruction instead of a
+// mostly-empty 128-row tile.  Token-major (EPI_NORMAL, large M with uniform
+// weight-block scales): 128 tokens on M / the TMEM lanes and 128 / 192 / 256
+// weight rows on N, so each lane's slice scale is one scalar.
 //
 // Warp roles (one CTA per SM, persistent over work units):
-//   warp 0        TMA producer for the weight operand (A ring); for FP8 x FP8
-//                 it also loads the B operand of the same slice
-//   warp 1        TMEM allocator + tcgen05.mma issuer (one elected lane)
-//   warp 2        with per-slice promotion, a second MMA issuer: warps 1
-//                 and 2 take the even and odd K slices (each slice has its
-//                 own TMEM buffer), so one warp's barrier waits never leave
-//                 the tensor pipe idle
-//   warp 3        bf16 kinds: TMA producer for the B operand (bf16 tokens);
-//                 scale loader: per 128-wide K slice, the column scales
-//                 As(m, kb) (times the tile's Ws(kb) when it is uniform) and,
-//                 when it is not, the per-row Ws(n, kb), into a shared ring
-//                 (token-major: As of the 128 token rows and Ws of the tile's
-//                 weight blocks); the epilogue never waits on a global load
-//   warps 4..     epilogue, one or two warpgroups splitting the token columns:
-//                 TMEM -> registers, scale promotion (one FFMA per element),
-//                 output
+//   warp 0        TMA producer for the A operand ring; for FP8 x FP8 it also
+//                 loads the B operand of the same slice onto the same barrier
+//   warps 1, 2    tcgen05.mma issuers (one elected lane each; warp 1 also
+//                 owns the TMEM allocation).  One thread blocks ~100 cycles
+//                 per instruction, so two issuers take alternate K slices:
+//                 with per-slice promotion every slice has its own TMEM
+//                 buffer; whole-K kinds give each unit a pair of
+//                 accumulators that the epilogue adds
+//   warp 3        scale loader, four slices ahead into a shared ring: the
+//                 column scales As(m, kb) (times Ws(kb) when uniform over the
+//                 tile) and, when not, the per-row Ws(n, kb); token-major:
+//                 As of the 128 token rows and Ws of the tile's weight
+//                 blocks; MXFP4: the slice's ue8m0 bytes.  For the bf16 kinds
+//                 it also issues the B-operand (bf16 token) TMA.  The
+//                 epilogue never waits on a global load
+//   warps 4..     epilogue, one to four warpgroups splitting the columns:
+//                 TMEM -> registers, scale promotion (packed FMA), output
 //   last 8 warps  (bf16 kinds only) weight decode, one thread per weight
 //                 row: e4m3 -> bf16 or e2m1 x 2^(e-127) -> bf16 from the
 //                 shared tile into a 4-slot TMEM ring that the MMA reads as
 //                 its A operand (no bf16 copy of the weights in shared
-//                 memory); for MXFP4 the scale warp stages each slice's ue8m0
-//                 bytes in a shared ring ahead of the decode
+//                 memory)
 //
 // Block scales ("[XPU] block-FP8 linear via torch scaled_mm": activations
 // BlockWise1x128, weights BlockWise128x128 or 1x128) are not powers of two, so
