@@ -10,8 +10,10 @@
 // weight rows on N, so each lane's slice scale is one scalar.
 //
 // Warp roles (one CTA per SM, persistent over work units):
-//   warp 0        TMA producer for the A operand ring; for FP8 x FP8 it also
-//                 loads the B operand of the same slice onto the same barrier
+//   warp 0        TMA producer: lane 0 loads the A operand ring (for FP8 x
+//                 FP8 also the B operand of the same slice, onto the same
+//                 barrier); for the bf16 kinds lane 1 loads the B operand
+//                 (bf16 tokens) into its own ring
 //   warps 1, 2    tcgen05.mma issuers (one elected lane each; warp 1 also
 //                 owns the TMEM allocation).  One thread blocks ~100 cycles
 //                 per instruction, so two issuers take alternate K slices:
@@ -22,12 +24,11 @@
 //                 column scales As(m, kb) (times Ws(kb) when uniform over the
 //                 tile) and, when not, the per-row Ws(n, kb); token-major:
 //                 As of the 128 token rows and Ws of the tile's weight
-//                 blocks; MXFP4: the slice's ue8m0 bytes.  For the bf16 kinds
-//                 it also issues the B-operand (bf16 token) TMA.  The
-//                 epilogue never waits on a global load
+//                 blocks; MXFP4: the slice's ue8m0 bytes.  The epilogue
+//                 never waits on a global load
 //   warps 4..     epilogue, one to four warpgroups splitting the columns:
 //                 TMEM -> registers, scale promotion (packed FMA), output
-//   last 8 warps  (bf16 kinds only) weight decode, one thread per weight
+//   last 8 / 16   (bf16 kinds only) weight decode, one thread per weight
 //                 row: e4m3 -> bf16 or e2m1 x 2^(e-127) -> bf16 from the
 //                 shared tile into a 4-slot TMEM ring that the MMA reads as
 //                 its A operand (no bf16 copy of the weights in shared
@@ -113,7 +114,12 @@ struct Layout {
   static constexpr int EW = (KIND == KIND_F8F8 && BT >= 192) ? BT / 64 : (BT >= 128 ? 2 : 1);
   static constexpr int COLS = BT / EW;                     // token columns per epilogue WG
   static constexpr int CONV_WARP0 = 4 + 4 * EW;
-  static constexpr int NCV = (KIND == KIND_F8F8) ? 0 : 8;  // weight-decode warps
+  // weight-decode warps, in groups of eight (one thread per weight row and
+  // K half).  MXFP4 tiles of up to 64 token columns run two groups that take
+  // alternate K slices: one group's decode is latency-bound (its integer ALU
+  // work leaves the pipe half idle)
+  static constexpr int NDG = (KIND == KIND_MXW && BT <= 64) ? 2 : 1;
+  static constexpr int NCV = (KIND == KIND_F8F8) ? 0 : 8 * NDG;
   static constexpr int kThreads = 128 * (1 + EW) + 32 * NCV;
   static constexpr int A_BYTES = (KIND == KIND_MXW) ? 128 * 64 : 128 * 128;
   static constexpr int B_BYTES = BT * 128 * ((KIND == KIND_F8F8) ? 1 : 2);
@@ -308,6 +314,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   using L = Layout<KIND, BT, EPI>;
   static_assert(KIND != KIND_F8F8 || PROMOTE, "FP8 x FP8 slices are always promoted (two issuers rely on it)");
+  static_assert(PROMOTE || L::STG == 16, "whole-K epilogue reads 16-column chunks");
   constexpr int AS = L::AS, BS = L::BS, CS = L::CS, EW = L::EW, COLS = L::COLS;
   constexpr int SSL = L::SSLOTS, STG = L::STG, GRP = L::GRP, NB = L::NBUF;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -346,14 +353,14 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < AS; ++i) {
       mbar_init(&a_full[i], 1);
-      mbar_init(&a_empty[i], KIND == KIND_F8F8 ? 1 : L::NCV);
+      mbar_init(&a_empty[i], KIND == KIND_F8F8 ? 1 : 8);   // one decode group per slice
     }
     for (int i = 0; i < BS; ++i) {
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < CS; ++i) {
-      mbar_init(&c_full[i], L::NCV);
+      mbar_init(&c_full[i], 8);
       mbar_init(&c_empty[i], 1);
     }
     for (int i = 0; i < NB; ++i) {
@@ -362,7 +369,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     }
     for (int i = 0; i < SSL; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], KIND == KIND_MXW ? L::NCV : 4 * EW);
+      mbar_init(&s_empty[i], KIND == KIND_MXW ? 8 : 4 * EW);
     }
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
@@ -419,6 +426,31 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         WaitCtx dw{p.status, &zero, 1000000000ull};
         const uint32_t first = it > static_cast<uint32_t>(AS) ? it - AS : 0;
         for (uint32_t i = first; i < it; ++i) mbar_wait(&a_full[i % AS], (i / AS) & 1, dw);
+      }
+    } else if (lane == 1 && KIND != KIND_F8F8 && !p.inject_stall) {
+      // bf16 kinds: the B operand (bf16 tokens, two 64-column halves) of
+      // every slice, in slice order, into its own ring released by the MMA.
+      // It runs apart from the scale loader so that the scale ring (which
+      // the MXFP4 decode waits on) is not held back by the B ring's depth.
+      uint32_t itb = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit U = get_unit<EPI, BT>(p, u);
+        const CUtensorMap* mb = &maps.b[U.bvar];
+        for (int kb = U.kb0; kb < U.kb1; ++kb, ++itb) {
+          const int sb = itb % BS;
+          if (!mbar_wait(&b_empty[sb], ((itb / BS) & 1) ^ 1, wc)) goto prod_b_done;
+          uint8_t* dst = sB + sb * L::B_BYTES;
+          mbar_expect_tx(&b_full[sb], U.brows * 256);
+          tma_load_2d(dst, mb, &b_full[sb], kb * 128, U.brow);
+          tma_load_2d(dst + U.brows * 128, mb, &b_full[sb], kb * 128 + 64, U.brow);
+        }
+      }
+    prod_b_done:
+      if (*abort_flag) {
+        volatile int zero = 0;
+        WaitCtx dw{p.status, &zero, 1000000000ull};
+        const uint32_t first = itb > static_cast<uint32_t>(BS) ? itb - BS : 0;
+        for (uint32_t i = first; i < itb; ++i) mbar_wait(&b_full[i % BS], (i / BS) & 1, dw);
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -524,35 +556,9 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       }
     }
   } else if (warp == 3) {
-    // ------------------------------------- scale loader (+ bf16 B operand)
-    // bf16 kinds: this warp also loads the B operand (bf16 tokens, two
-    // 64-column halves) of every slice, in slice order, just before
-    // publishing the slice's scales; the B ring is released by the MMA
-    uint32_t itb = 0;
-    auto produce_b = [&](const Unit& U, int kb) -> bool {
-      if (KIND == KIND_F8F8) return true;
-      if (!p.inject_stall) {
-        const int sb = itb % BS;
-        if (!mbar_wait(&b_empty[sb], ((itb / BS) & 1) ^ 1, wc)) return false;
-        if (lane == 0) {
-          uint8_t* dst = sB + sb * L::B_BYTES;
-          const CUtensorMap* mb = &maps.b[U.bvar];
-          mbar_expect_tx(&b_full[sb], U.brows * 256);
-          tma_load_2d(dst, mb, &b_full[sb], kb * 128, U.brow);
-          tma_load_2d(dst + U.brows * 128, mb, &b_full[sb], kb * 128 + 64, U.brow);
-        }
-        __syncwarp();
-      }
-      ++itb;
-      return true;
-    };
+    // ------------------------------------------------------ scale loader
     if (KIND == KIND_F8W && !PROMOTE) {
-      // per-tensor weights: no slice scales, only the B operand
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const Unit U = get_unit<EPI, BT>(p, u);
-        for (int kb = U.kb0; kb < U.kb1; ++kb)
-          if (!produce_b(U, kb)) goto scale_done;
-      }
+      // per-tensor weights: no slice scales
     } else if (KIND == KIND_MXW) {
       // ue8m0 bytes of each slice (4 groups of 32 along K per weight row),
       // four slices ahead in registers; rows of a ragged tail clamp to the
@@ -586,7 +592,6 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             if (kb + q < U.kb1) {
-              if (!produce_b(U, kb + q)) goto mx_done;
               const int slot = is % SSL;
               if (!mbar_wait(&s_empty[slot], ((is / SSL) & 1) ^ 1, wc)) goto mx_done;
 #pragma unroll
@@ -697,7 +702,6 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             if (kb + q < U.kb1) {
-              if (!produce_b(U, kb + q)) goto scale_done;
               if (!publish(ra[q], rw[q], ru[q])) goto scale_done;
               if (kb + q + 4 < U.kb1) fetch(kb + q + 4, ra[q], rw[q], ru[q]);
             }
@@ -705,14 +709,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         }
       }
     }
-  scale_done:
-    if (KIND != KIND_F8F8 && *abort_flag && !p.inject_stall) {
-      // let every B copy already issued land before the CTA goes away
-      volatile int zero = 0;
-      WaitCtx dw{p.status, &zero, 1000000000ull};
-      const uint32_t first = itb > static_cast<uint32_t>(BS) ? itb - BS : 0;
-      for (uint32_t i = first; i < itb; ++i) mbar_wait(&b_full[i % BS], (i / BS) & 1, dw);
-    }
+  scale_done:;
   } else if (warp >= L::CONV_WARP0) {
     // ------------------------------------------- weight decode to bf16
     // Thread = weight row of the tile = TMEM lane; the two warps of a lane
@@ -721,7 +718,9 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     // stores 32 columns of bf16 pairs into the TMEM ring slot, which the
     // MMA then reads as its A operand.
     if constexpr (KIND != KIND_F8F8) {
-      const int half = (warp - L::CONV_WARP0) >> 2;
+      const int cw = warp - L::CONV_WARP0;
+      const uint32_t grp = static_cast<uint32_t>(cw >> 3);   // takes slices with ia % NDG == grp
+      const int half = (cw >> 2) & 1;
       const int r = (warp & 3) * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
                              L::C_TCOL + half * 32;
@@ -729,6 +728,10 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
         for (int kb = U.kb0; kb < U.kb1; ++kb, ++ia, ++ic) {
+          if (L::NDG > 1 && ia % L::NDG != grp) {
+            if (KIND == KIND_MXW) ++is;   // the other group's scale slot
+            continue;
+          }
           const int sa = ia % AS, sc = ic % CS;
           if (!mbar_wait(&a_full[sa], (ia / AS) & 1, wc)) goto conv_done;
           if (!mbar_wait(&c_empty[sc], ((ic / CS) & 1) ^ 1, wc)) goto conv_done;
@@ -942,6 +945,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       const int ngr = (colv + GRP - 1) / GRP;              // column groups with valid tokens
       float acc[COLS];
       float fscale = 1.f;
+      uint32_t buf0 = 0, buf1 = 0;   // whole-K kinds: the unit's accumulator pair
+      bool two = false;
       if (PROMOTE) {
 #pragma unroll
         for (int j = 0; j < COLS; ++j) acc[j] = 0.f;
@@ -1005,29 +1010,14 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         // the unit's two accumulators (one per MMA issuer); the second is
         // unwritten when the unit has a single K slice
         const uint32_t tb0 = 2 * au, tb1 = 2 * au + 1;
-        const uint32_t buf0 = tb0 % NB, buf1 = tb1 % NB;
-        const bool two = U.kb1 - U.kb0 >= 2;
+        buf0 = tb0 % NB;
+        buf1 = tb1 % NB;
+        two = U.kb1 - U.kb0 >= 2;
         if (!mbar_wait(&t_full[buf0], (tb0 / NB) & 1, wc)) goto epi_done;
         if (!mbar_wait(&t_full[buf1], (tb1 / NB) & 1, wc)) goto epi_done;
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < COLS / GRP; ++c) {
-          if (c < ngr) {
-            tmem_ld<GRP>(tmem_base + lane_addr + buf0 * L::BSTRIDE + col0 + c * GRP, &acc[c * GRP]);
-            if (two) {
-              float v[GRP];
-              tmem_ld<GRP>(tmem_base + lane_addr + buf1 * L::BSTRIDE + col0 + c * GRP, v);
-#pragma unroll
-              for (int j = 0; j < GRP; ++j) acc[c * GRP + j] += v[j];
-            }
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&t_empty[buf0]);
-          mbar_arrive(&t_empty[buf1]);
-        }
+        // the accumulators are read one staging chunk at a time below, so
+        // no register array holds the tile's columns
         ++au;
       }
       // ------------------------------------------------------- output
@@ -1051,8 +1041,21 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < COLS / STG; ++c) {
           if (c * STG < colv) {
+            if constexpr (PROMOTE) {
 #pragma unroll
-            for (int j = 0; j < STG; ++j) stg[j * 128 + et] = acc[c * STG + j] * fscale;
+              for (int j = 0; j < STG; ++j) stg[j * 128 + et] = acc[c * STG + j] * fscale;
+            } else {
+              float v0[STG];
+              tmem_ld<STG>(tmem_base + lane_addr + buf0 * L::BSTRIDE + col0 + c * STG, v0);
+              if (two) {
+                float v1[STG];
+                tmem_ld<STG>(tmem_base + lane_addr + buf1 * L::BSTRIDE + col0 + c * STG, v1);
+#pragma unroll
+                for (int j = 0; j < STG; ++j) v0[j] += v1[j];
+              }
+#pragma unroll
+              for (int j = 0; j < STG; ++j) stg[j * 128 + et] = v0[j] * fscale;
+            }
             if (!group_sync(&epi_bar[g], eph, wc)) goto epi_done;
             if (EPI == EPI_DENSE) {
               for (int jj = et >> 5; jj < STG; jj += 4) {
@@ -1126,6 +1129,15 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
               }
             }
             if (!group_sync(&epi_bar[g], eph, wc)) goto epi_done;
+          }
+        }
+        if constexpr (!PROMOTE) {
+          // every chunk of the accumulator pair has been read
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&t_empty[buf0]);
+            mbar_arrive(&t_empty[buf1]);
           }
         }
       }
