@@ -580,6 +580,10 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
       p.mx_ld = red / 32;
       p.mx_cols = static_cast<int>(red / 32);
       p.mx_rows_total = static_cast<int64_t>(E) * rows;
+      {
+        const uintptr_t sb = reinterpret_cast<uintptr_t>(wsc);
+        p.mx_align = ((p.mx_ld % 4) == 0 && (sb % 4) == 0) ? 4 : (((p.mx_ld % 2) == 0 && (sb % 2) == 0) ? 2 : 1);
+      }
       p.block_n = 0;
     }
     p.bias = stage == 0 ? w1_bias : w2_bias;

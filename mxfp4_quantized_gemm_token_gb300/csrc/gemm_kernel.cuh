@@ -93,6 +93,7 @@ struct GemmParams {
   int64_t mx_ld;
   int mx_cols;
   int64_t mx_rows_total;
+  int mx_align;       // 4, 2 or 1: alignment of every row of the ue8m0 scales
   const void* bias;
   int bias_dtype;
   int64_t bias_e;
@@ -561,45 +562,58 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       // per-tensor weights: no slice scales
     } else if (KIND == KIND_MXW) {
       // ue8m0 bytes of each slice (4 groups of 32 along K per weight row),
-      // four slices ahead in registers; rows of a ragged tail clamp to the
-      // last row and columns past K read 127 (2^0; the data there is zero)
+      // MLA slices ahead in registers; rows of a ragged tail clamp to the
+      // last row and columns past K read 127 (2^0; the data there is zero).
+      // With even row strides a row's four bytes are two 16-bit loads whose
+      // halves are joined only when the slice is published, so no fetch
+      // waits on its loads; other strides and a ragged K end join the bytes
+      // at once.
+      constexpr int MLA = 4;
       uint32_t is = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
-        uint32_t rx[4][4];
-        auto fetch = [&](int kb, uint32_t* x) {
+        uint32_t rh[MLA][8];
+        auto fetch = [&](int kb, uint32_t* h) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int r = lane + 32 * i;
             int64_t grow = (EPI == EPI_SILU) ? static_cast<int64_t>(r < 64 ? U.wrow0 + r : U.wrow1 + (r - 64))
                                              : static_cast<int64_t>(U.wrow0) + r;
             if (grow >= p.mx_rows_total) grow = p.mx_rows_total - 1;
-            const uint8_t* rowp = p.mx_scale + grow * p.mx_ld;
-            uint32_t v = 0;
+            const uint8_t* rowp = p.mx_scale + grow * p.mx_ld + kb * 4;
+            if (p.mx_align >= 2 && kb * 4 + 4 <= p.mx_cols) {
+              const uint16_t* hp = reinterpret_cast<const uint16_t*>(rowp);
+              h[2 * i] = __ldg(hp);
+              h[2 * i + 1] = __ldg(hp + 1);
+            } else {
+              uint32_t v = 0;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int col = kb * 4 + c;
-              const uint32_t b = (col < p.mx_cols) ? __ldg(rowp + col) : 127u;
-              v |= b << (8 * c);
+              for (int c = 0; c < 4; ++c) {
+                const int col = kb * 4 + c;
+                const uint32_t b = (col < p.mx_cols) ? __ldg(rowp + c) : 127u;
+                v |= b << (8 * c);
+              }
+              h[2 * i] = v & 0xFFFFu;
+              h[2 * i + 1] = v >> 16;
             }
-            x[i] = v;
           }
         };
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (U.kb0 + q < U.kb1) fetch(U.kb0 + q, rx[q]);
-        for (int kb = U.kb0; kb < U.kb1; kb += 4) {
+        for (int q = 0; q < MLA; ++q)
+          if (U.kb0 + q < U.kb1) fetch(U.kb0 + q, rh[q]);
+        for (int kb = U.kb0; kb < U.kb1; kb += MLA) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < MLA; ++q) {
             if (kb + q < U.kb1) {
               const int slot = is % SSL;
               if (!mbar_wait(&s_empty[slot], ((is / SSL) & 1) ^ 1, wc)) goto mx_done;
 #pragma unroll
-              for (int i = 0; i < 4; ++i) sMx[slot * 128 + lane + 32 * i] = rx[q][i];
+              for (int i = 0; i < 4; ++i)
+                sMx[slot * 128 + lane + 32 * i] = rh[q][2 * i] | (rh[q][2 * i + 1] << 16);
               __syncwarp();
               if (lane == 0) mbar_arrive(&s_full[slot]);
               ++is;
-              if (kb + q + 4 < U.kb1) fetch(kb + q + 4, rx[q]);
+              if (kb + q + MLA < U.kb1) fetch(kb + q + MLA, rh[q]);
             }
           }
         }
