@@ -12,12 +12,14 @@ namespace mxq {
 // the block's token slots sorted_ids[mb*block_m + m] and the compact row
 // offsets[mb]; this kernel produces them.  One CTA of 1024 threads:
 //   1. histogram of slots per expert (shared-memory atomics);
-//   2. exclusive scans: first block and first compact row of each expert;
+//   2. exclusive scans of the per-expert block and slot counts: warp
+//      shuffles, then a scan of the 32 warp totals, 1024 experts per pass;
 //   3. the block table (expert_ids, offsets);
 //   4. a stable ranking of the slots, 1024 at a time in slot order: inside a
 //      warp, lanes with the same expert find each other with match.any and
-//      rank by lane; across warps, per-warp counts in shared memory give the
-//      offset; a running count per expert carries over between chunks.
+//      rank by lane; per-warp counts in shared memory are turned into
+//      per-warp starting positions by one pass per expert over the 32 warps,
+//      which also carries the running count per expert to the next chunk.
 // The result is unique (stable order), so it is compared bit for bit.
 __global__ void __launch_bounds__(1024) moe_align_kernel(const int32_t* __restrict__ ids, int S,
                                                          int E, int BM, int cap,
@@ -32,6 +34,7 @@ __global__ void __launch_bounds__(1024) moe_align_kernel(const int32_t* __restri
   int* pos_start = blk_start + E;
   int* run = pos_start + E;
   int* wcnt = run + E;   // [32][E]
+  __shared__ int wsum_b[32], wsum_p[32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   for (int i = tid; i < E; i += 1024) {
@@ -55,18 +58,64 @@ __global__ void __launch_bounds__(1024) moe_align_kernel(const int32_t* __restri
   if (bad) atomicOr(status, kStatusBadIndex);
   __syncthreads();
 
-  if (tid == 0) {
-    int b = 0, pos = 0;
-    for (int e = 0; e < E; ++e) {
-      blk_start[e] = b;
-      pos_start[e] = pos;
-      b += (cnt[e] + BM - 1) / BM;
-      pos += cnt[e];
+  // exclusive scans: first block and first compact row of each expert
+  int carry_b = 0, carry_p = 0;
+  for (int e0 = 0; e0 < E; e0 += 1024) {
+    const int e = e0 + tid;
+    const int c = (e < E) ? cnt[e] : 0;
+    const int ob = (c + BM - 1) / BM, op = c;
+    int vb = ob, vp = op;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int tb = __shfl_up_sync(0xffffffffu, vb, d);
+      const int tp = __shfl_up_sync(0xffffffffu, vp, d);
+      if (lane >= d) {
+        vb += tb;
+        vp += tp;
+      }
     }
-    *num_blocks = b;
-    offsets[b] = pos;
+    if (lane == 31) {
+      wsum_b[warp] = vb;
+      wsum_p[warp] = vp;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int xb = wsum_b[lane], xp = wsum_p[lane];
+      int ib = xb, ip = xp;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int tb = __shfl_up_sync(0xffffffffu, ib, d);
+        const int tp = __shfl_up_sync(0xffffffffu, ip, d);
+        if (lane >= d) {
+          ib += tb;
+          ip += tp;
+        }
+      }
+      wsum_b[lane] = ib - xb;   // exclusive over warps
+      wsum_p[lane] = ip - xp;
+    }
+    __syncthreads();
+    if (e < E) {
+      blk_start[e] = carry_b + wsum_b[warp] + vb - ob;
+      pos_start[e] = carry_p + wsum_p[warp] + vp - op;
+    }
+    // this pass's totals: the last expert's inclusive values
+    const int tot_b = __shfl_sync(0xffffffffu, vb, 31) + wsum_b[warp];
+    const int tot_p = __shfl_sync(0xffffffffu, vp, 31) + wsum_p[warp];
+    __syncthreads();
+    if (tid == 1023) {
+      wsum_b[0] = tot_b;
+      wsum_p[0] = tot_p;
+    }
+    __syncthreads();
+    carry_b += wsum_b[0];
+    carry_p += wsum_p[0];
+    __syncthreads();
   }
-  __syncthreads();
+  if (tid == 0) {
+    *num_blocks = carry_b;
+    offsets[carry_b] = carry_p;
+  }
   for (int e = tid; e < E; e += 1024) {
     const int nb = (cnt[e] + BM - 1) / BM;
     for (int j = 0; j < nb; ++j) {
@@ -86,20 +135,25 @@ __global__ void __launch_bounds__(1024) moe_align_kernel(const int32_t* __restri
     const bool leader = (__ffs(peers) - 1) == lane;
     if (valid && leader) wcnt[warp * E + e] = __popc(peers);
     __syncthreads();
-    if (valid) {
-      int pos = run[e] + rank;
-      for (int w = 0; w < warp; ++w) pos += wcnt[w * E + e];
-      sorted_ids[static_cast<int64_t>(blk_start[e]) * BM + pos] = s;
-    }
-    __syncthreads();
+    // per expert: counts of the 32 warps -> each warp's first position
     for (int ee = tid; ee < E; ee += 1024) {
-      int t = 0;
-      for (int w = 0; w < 32; ++w) t += wcnt[w * E + ee];
-      run[ee] += t;
+      int acc = run[ee];
+#pragma unroll 8
+      for (int w = 0; w < 32; ++w) {
+        const int t = wcnt[w * E + ee];
+        wcnt[w * E + ee] = acc;
+        acc += t;
+      }
+      run[ee] = acc;
     }
     __syncthreads();
-    if (valid && leader) wcnt[warp * E + e] = 0;
+    if (valid)
+      sorted_ids[static_cast<int64_t>(blk_start[e]) * BM + wcnt[warp * E + e] + rank] = s;
     __syncthreads();
+    if (base + 1024 < S) {
+      for (int i = tid; i < 32 * E; i += 1024) wcnt[i] = 0;
+      __syncthreads();
+    }
   }
 }
 
