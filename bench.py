@@ -558,7 +558,8 @@ def run_workloads(args, local):
                     gms = _graph_timed_calls(f, reps, flush)
                     byts = touched * per_expert + T * K * 4
                     flops = T * topk * (2 * K * 2 * N + 2 * N * K)
-                    emit({"T": T, "routing": routing, "experts_touched": touched, "block_m": bm,
+                    bm_used = bm if bm else (32 if T * topk <= 16 * E else 64)
+                    emit({"T": T, "routing": routing, "experts_touched": touched, "block_m": bm_used,
                           "us": ms * 1e3, "us_graph": None if gms is None else gms * 1e3, "TFLOPs": flops / ms / 1e9, "GBs": byts / ms / 1e6,
                           "hbm_frac": byts / ms / 1e6 / hbm})
     return 0
@@ -597,7 +598,8 @@ def run_ablation(args, local):
                     tw, ids = tw.to(dev), ids.to(dev)
                     line = {"workload": "moe_ablation", "kind": kind, "T": T, "routing": routing,
                             "experts_touched": touched, "avg_m": max(1, T * topk // E),
-                            "block_m": args.block_m, "small_m_max": 16}
+                            "block_m": args.block_m or (32 if T * topk <= 16 * E else 64),
+                            "small_m_max": 16}
                     for name, force in modes:
                         mxq.set_option(_lib.OPT_FORCE_PATH, force)
                         f = lambda: mxq.fused_experts(x, w1, s1, w2, s2, tw, ids,
@@ -624,7 +626,8 @@ def main():
                     help="measure the vendor FP8 GEMM burst rate (8192^3) and exit")
     ap.add_argument("--workload", default="",
                     help="comma list of pertensor, block1x128, moe_fp8, moe_mxfp4 (tables only)")
-    ap.add_argument("--block-m", type=int, default=64)
+    ap.add_argument("--block-m", type=int, default=0,
+                    help="MoE tokens per expert block; 0 = the library's choice")
     ap.add_argument("--profile", type=int, default=0,
                     help="run 3 launches of quant + GEMM at this M only (for ncu)")
     ap.add_argument("--profile-moe", default="",

@@ -218,7 +218,9 @@ mxq_status mxq_moe_align_block(const int32_t* topk_ids, int64_t T, int32_t topk,
  *     w2 e2m1x2 [E, K, N/2],  w2_scale ue8m0 [E, K, N/32]
  *   w1_bias fp32 [E, 2N] or NULL; w2_bias fp32 [E, K] or NULL
  *   topk_weights fp32 [T, topk]; topk_ids int32 [T, topk]
- *   block_m  in {16, 32, 64, 128}: tokens per expert block
+ *   block_m  in {16, 32, 64, 128}: tokens per expert block; 0 = the
+ *            library's choice (32 when S = T*topk <= 16*E, else 64), the
+ *            same value for mxq_fused_experts_workspace_size
  *   out      bf16 [T, K], row stride ldo
  *   workspace: mxq_fused_experts_workspace_size bytes, 256-byte aligned
  */

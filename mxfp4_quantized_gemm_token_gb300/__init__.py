@@ -207,9 +207,12 @@ def moe_align_block(topk_ids: torch.Tensor, num_experts: int, block_m: int, cap=
 
 
 def fused_experts(hidden, w1, w1_scale, w2, w2_scale, topk_weights, topk_ids,
-                  wtype=W_FP8_BLOCK128, w1_bias=None, w2_bias=None, block_m: int = 64,
+                  wtype=W_FP8_BLOCK128, w1_bias=None, w2_bias=None, block_m: int = 0,
                   workspace=None, checkpoints: bool = False):
-    """Routed MoE: align, stage 1 (+ SiLU-and-mul), stage 2, top-k combine."""
+    """Routed MoE: align, stage 1 (+ SiLU-and-mul), stage 2, top-k combine.
+
+    block_m: tokens per expert block (16, 32, 64, 128), or 0 for the
+    library's choice (32 when T*topk <= 16*E, else 64)."""
     _need_cuda(hidden, w1, w1_scale, w2, w2_scale, topk_weights, topk_ids, w1_bias, w2_bias)
     lib = _lib_handle()
     T, K = hidden.shape

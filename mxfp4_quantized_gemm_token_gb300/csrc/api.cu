@@ -432,6 +432,16 @@ struct MoeWs {
   int64_t S, cap;
 };
 
+// block_m 0: the library's choice.  Expert blocks of 32 slots let the
+// weight-decode warps of the FP8-block GEMM run as two groups (the registers
+// of a 64-wide tile do not allow it); when experts average more than 16
+// slots, 32-slot blocks would split experts and stream their weights twice,
+// so 64.  (MXFP4 runs two decode groups at either width.)
+int32_t resolve_block_m(int32_t block_m, int64_t S, int32_t E) {
+  if (block_m != 0) return block_m;
+  return S <= 16 * static_cast<int64_t>(E) ? 32 : 64;
+}
+
 MoeWs moe_ws(int64_t T, int64_t K, int32_t E, int64_t N, int32_t topk, int32_t block_m) {
   MoeWs w;
   w.S = T * topk;
@@ -469,8 +479,9 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
     return fail(MXQ_ERR_INVALID_ARG, "NULL tensor argument");
   if (E < 1 || E > 1024) return fail(MXQ_ERR_UNSUPPORTED, "E must be in [1, 1024]");
   if (topk > E) return fail(MXQ_ERR_INVALID_ARG, "topk must be <= E");
+  block_m = resolve_block_m(block_m, T * topk, E);
   if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128)
-    return fail(MXQ_ERR_UNSUPPORTED, "block_m must be 16, 32, 64 or 128");
+    return fail(MXQ_ERR_UNSUPPORTED, "block_m must be 0 (library choice), 16, 32, 64 or 128");
   if (wtype != MXQ_W_FP8_BLOCK128 && wtype != MXQ_W_MXFP4)
     return fail(MXQ_ERR_UNSUPPORTED, "wtype must be MXQ_W_FP8_BLOCK128 or MXQ_W_MXFP4");
   if (ldh < K || ldo < K) return fail(MXQ_ERR_INVALID_ARG, "row strides below K");
@@ -620,9 +631,9 @@ extern "C" mxq_status mxq_fused_experts_workspace_size(int64_t T, int64_t K, int
                                                        int32_t topk, int32_t block_m,
                                                        int32_t wtype, size_t* bytes) {
   (void)wtype;
-  if (!bytes || T < 0 || K <= 0 || N <= 0 || topk <= 0 || E < 1 || block_m <= 0)
+  if (!bytes || T < 0 || K <= 0 || N <= 0 || topk <= 0 || E < 1 || block_m < 0)
     return fail(MXQ_ERR_INVALID_ARG, "bad sizes or NULL result pointer");
-  *bytes = moe_ws(T, K, E, N, topk, block_m).total;
+  *bytes = moe_ws(T, K, E, N, topk, resolve_block_m(block_m, T * topk, E)).total;
   return MXQ_OK;
 }
 

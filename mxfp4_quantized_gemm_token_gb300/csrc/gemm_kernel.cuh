@@ -116,10 +116,12 @@ struct Layout {
   static constexpr int COLS = BT / EW;                     // token columns per epilogue WG
   static constexpr int CONV_WARP0 = 4 + 4 * EW;
   // weight-decode warps, in groups of eight (one thread per weight row and
-  // K half).  MXFP4 tiles of up to 64 token columns run two groups that take
-  // alternate K slices: one group's decode is latency-bound (its integer ALU
-  // work leaves the pipe half idle)
-  static constexpr int NDG = (KIND == KIND_MXW && BT <= 64) ? 2 : 1;
+  // K half).  Two groups that take alternate K slices where the registers
+  // allow it (MXFP4 tiles of up to 64 token columns, FP8-block tiles of 32):
+  // one group's decode is latency-bound (its integer ALU work leaves the
+  // pipe half idle)
+  static constexpr int NDG =
+      ((KIND == KIND_MXW && BT <= 64) || (KIND == KIND_F8W && BT <= 32)) ? 2 : 1;
   static constexpr int NCV = (KIND == KIND_F8F8) ? 0 : 8 * NDG;
   static constexpr int kThreads = 128 * (1 + EW) + 32 * NCV;
   static constexpr int A_BYTES = (KIND == KIND_MXW) ? 128 * 64 : 128 * 128;

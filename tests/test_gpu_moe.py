@@ -83,7 +83,7 @@ def run_moe(oracle, wtype, E, N, K, x, tw, ids, block_m, seed=1, bias=False, che
     return out
 
 
-@pytest.mark.parametrize("block_m", [16, 32, 64, 128])
+@pytest.mark.parametrize("block_m", [0, 16, 32, 64, 128])
 def test_fused_fp8_small(oracle, block_m):
     E, N, K, T, topk = 8, 128, 256, 13, 2
     x = synth.activations(T, K, seed=3, scale_div=10)
@@ -98,7 +98,7 @@ def test_fused_fp8_ragged_dims_and_many_tokens(oracle):
     run_moe(oracle, W_FP8, E, N, K, x, tw, ids, 32)
 
 
-@pytest.mark.parametrize("block_m", [16, 64])
+@pytest.mark.parametrize("block_m", [0, 16, 64])
 def test_fused_mxfp4_bias(oracle, block_m):
     E, N, K, T, topk = 4, 160, 288, 9, 4
     x = synth.activations(T, K, seed=7, scale_div=10)
