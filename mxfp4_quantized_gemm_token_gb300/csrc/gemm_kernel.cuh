@@ -462,12 +462,17 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     // promotion every slice has its own TMEM buffer and two issuing warps
     // take every other slice.
     {
-      // Two issuers.  Promoted kinds: every slice has its own buffer and
-      // the issuers take alternate slices.  Whole-K kinds: each unit has a
-      // pair of accumulators, issuer i summing the unit's slices l with
-      // l % 2 == i into buffer (2 * unit + i) % NB; the epilogue adds the
-      // pair.  An issuer with no slice in a unit (one-slice units) hands
-      // over its buffer unwritten, so every barrier phase stays in step.
+      // Two issuers, taking alternate slices of the CTA's slice sequence
+      // (global index ia, across units), so that issuer i consumes exactly
+      // the slices that decode group i fills when the decode runs as two
+      // groups; each of its ring waits then follows a fill of the same
+      // producer that is known to be complete, and no parity wait can see
+      // a phase one lap behind.  Promoted kinds: every slice has its own
+      // buffer.  Whole-K kinds: each unit has a pair of accumulators, issuer
+      // i summing its slices of the unit into buffer (2 * unit + i) % NB;
+      // the epilogue adds the pair.  An issuer with no slice in a unit (a
+      // one-slice unit whose slice is the other issuer's) hands over its
+      // buffer unwritten, so every barrier phase stays in step.
       constexpr uint32_t NISS = 2;
       const uint32_t mine = (warp == 1) ? 0u : 1u;
       uint32_t ia = 0, ib = 0, au = 0;
@@ -482,14 +487,15 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           const uint32_t tb = 2 * au + mine;
           ubuf = tb % NB;
           if (!mbar_wait_warp(&t_empty[ubuf], ((tb / NB) & 1) ^ 1, wc)) goto mma_done;
-          if (nsl <= static_cast<int>(mine)) {
+          if (nsl == 1 && ia % NISS != mine) {
             if (elect_one()) mma_commit(&t_full[ubuf]);
             __syncwarp();
           }
         }
+        bool first = true;   // this issuer's first slice of the unit
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
           const int l = kb - U.kb0;
-          const bool take = PROMOTE ? (ia % NISS == mine) : (static_cast<uint32_t>(l) % NISS == mine);
+          const bool take = ia % NISS == mine;
           if (!take) {
             ++ia;
             ++ib;
@@ -510,7 +516,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           tc_fence_after();
           const uint32_t d = tmem_base + buf * L::BSTRIDE;
           // accumulate except on the first K step of this issuer's first slice
-          const bool fresh = PROMOTE || static_cast<uint32_t>(l) == mine;
+          const bool fresh = PROMOTE || first;
+          first = false;
           const bool leader = elect_one();
           if (leader) {
           if (KIND == KIND_F8F8) {
@@ -955,6 +962,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float* stg = sOut + g * (STG * 128);
     uint32_t au = 0, is = 0, eph = 0;
+    uint32_t esl = 0;   // the CTA's slice count before this unit (issuer of a one-slice unit)
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit U = get_unit<EPI, BT>(p, u);
       const int colv = max(0, min(COLS, U.rows - col0));   // valid columns of this WG
@@ -962,6 +970,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       float acc[COLS];
       float fscale = 1.f;
       uint32_t buf0 = 0, buf1 = 0;   // whole-K kinds: the unit's accumulator pair
+      uint32_t rd0 = 0;              // the pair's first buffer to read
       bool two = false;
       if (PROMOTE) {
 #pragma unroll
@@ -1032,9 +1041,13 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         if (!mbar_wait(&t_full[buf0], (tb0 / NB) & 1, wc)) goto epi_done;
         if (!mbar_wait(&t_full[buf1], (tb1 / NB) & 1, wc)) goto epi_done;
         tc_fence_after();
+        // a one-slice unit's slice went to issuer (esl % 2); its buffer is the
+        // one to read (the other is unwritten)
+        rd0 = (!two && (esl & 1u)) ? buf1 : buf0;
         // the accumulators are read one staging chunk at a time below, so
         // no register array holds the tile's columns
         ++au;
+        esl += static_cast<uint32_t>(U.kb1 - U.kb0);
       }
       // ------------------------------------------------------- output
       {
@@ -1062,7 +1075,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
               for (int j = 0; j < STG; ++j) stg[j * 128 + et] = acc[c * STG + j] * fscale;
             } else {
               float v0[STG];
-              tmem_ld<STG>(tmem_base + lane_addr + buf0 * L::BSTRIDE + col0 + c * STG, v0);
+              tmem_ld<STG>(tmem_base + lane_addr + rd0 * L::BSTRIDE + col0 + c * STG, v0);
               if (two) {
                 float v1[STG];
                 tmem_ld<STG>(tmem_base + lane_addr + buf1 * L::BSTRIDE + col0 + c * STG, v1);

@@ -106,6 +106,19 @@ def test_fused_mxfp4_bias(oracle, block_m):
     run_moe(oracle, W_MX, E, N, K, x, tw, ids, block_m, bias=True)
 
 
+@pytest.mark.parametrize("wtype,block_m", [(W_MX, 32), (W_MX, 64), (W_FP8, 32)])
+def test_fused_odd_slice_units_two_decode_groups(oracle, wtype, block_m):
+    """K = N = 384: both stages reduce over three 128-wide slices, so the CTA's
+    slice sequence changes parity at every unit boundary, with several units
+    per CTA (64 experts x 6 or 3 tiles) and the weight decode split into two
+    groups taking alternate slices (the layouts where the MMA issuers and
+    the decode groups must agree on the alternation)."""
+    E, N, K, T, topk = 64, 384, 384, 96, 4
+    x = synth.activations(T, K, seed=21, scale_div=10)
+    tw, ids = synth.routing_uniform(T, E, topk, seed=22)
+    run_moe(oracle, wtype, E, N, K, x, tw, ids, block_m, bias=(wtype == W_MX))
+
+
 @pytest.mark.parametrize("wtype", [W_FP8, W_MX])
 def test_fused_single_slice_stages(oracle, wtype):
     """K = 128 and N = 64: both GEMM stages reduce over one 128-wide slice,
