@@ -79,8 +79,12 @@ enum {
   MXQ_OPT_NUM_SMS = 6,      /* persistent grid size cap; 0 = all SMs */
   MXQ_OPT_TILE_N = 7,       /* fp8_scaled_mm token-tile width: 0 auto, or 32, 64, 128,
                                256 (256 for FP8 activations only) */
-  MXQ_OPT_NORMAL_TILE = 8   /* fp8_scaled_mm weight-tile width when the tokens sit on
+  MXQ_OPT_NORMAL_TILE = 8,  /* fp8_scaled_mm weight-tile width when the tokens sit on
                                the MMA M side (large-M W8A8): 0 auto, 128, 192 or 256 */
+  MXQ_OPT_PDL = 9           /* 1 (default): kernels are launched with programmatic stream
+                               serialization, so a kernel's launch and prologue overlap the
+                               end of the previous kernel on the stream (each waits for it
+                               before touching global memory); 0: plain stream order */
 };
 
 const char* mxq_last_error(void);

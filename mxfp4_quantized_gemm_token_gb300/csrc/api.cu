@@ -29,7 +29,7 @@ mxq_status cuda_fail(cudaError_t e, const char* what) {
   return fail(MXQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-std::atomic<int64_t> g_opts[9] = {0, int64_t(1) << 30, 0, 2000000000LL, 0, 0, 0, 0, 0};
+std::atomic<int64_t> g_opts[10] = {0, int64_t(1) << 30, 0, 2000000000LL, 0, 0, 0, 0, 0, 1};
 
 std::mutex g_dev_mu;
 DeviceInfo g_devs[64];
@@ -132,7 +132,7 @@ extern "C" const char* mxq_last_error(void) { return g_err.c_str(); }
 extern "C" const char* mxq_version(void) { return "mxq 0.1 (sm_103a, tcgen05)"; }
 
 extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
-  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_NORMAL_TILE)
+  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_PDL)
     return fail(MXQ_ERR_INVALID_ARG, "unknown option " + std::to_string(opt));
   if (opt == MXQ_OPT_NORMAL_TILE && value != 0 && value != 128 && value != 192 && value != 256)
     return fail(MXQ_ERR_INVALID_ARG, "NORMAL_TILE is 0 (auto), 128, 192 or 256");
@@ -140,6 +140,8 @@ extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
       value != 256)
     return fail(MXQ_ERR_INVALID_ARG, "TILE_N is 0 (auto), 32, 64, 128 or 256");
   if (value < 0) return fail(MXQ_ERR_INVALID_ARG, "option values are non-negative");
+  if (opt == MXQ_OPT_PDL && value != 0 && value != 1)
+    return fail(MXQ_ERR_INVALID_ARG, "PDL is 0 (off) or 1 (on)");
   if (opt == MXQ_OPT_FORCE_PATH && value > 3)
     return fail(MXQ_ERR_INVALID_ARG,
                 "FORCE_PATH is 0 (per block), 1 (narrow), 2 (full width) or 3 (one path per layer)");
@@ -148,7 +150,7 @@ extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
 }
 
 extern "C" mxq_status mxq_get_option(int32_t opt, int64_t* value) {
-  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_NORMAL_TILE || value == nullptr)
+  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_PDL || value == nullptr)
     return fail(MXQ_ERR_INVALID_ARG, "unknown option or NULL value");
   *value = g_opts[opt].load();
   return MXQ_OK;

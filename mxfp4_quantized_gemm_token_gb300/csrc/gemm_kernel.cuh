@@ -389,6 +389,10 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the prologue above touches no global memory; from here on the previous
+  // kernel's results (tokens, scales, the expert-block table) are read
+  pdl_wait();
+  pdl_launch_dependents();
 
   const int total =
       p.grouped ? __ldg(p.num_blocks) * p.tiles_n : p.tiles_n * p.tiles_m * p.splits;

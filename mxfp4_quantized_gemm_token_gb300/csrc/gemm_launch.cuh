@@ -20,8 +20,8 @@ cudaError_t launch_gemm_inst(const GemmMaps& maps, const GemmParams& p, int grid
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  gemm_kernel<KIND, EPI, BT, PROMOTE><<<grid, L::kThreads, smem, stream>>>(maps, p);
-  return cudaGetLastError();
+  return launch_k(gemm_kernel<KIND, EPI, BT, PROMOTE>, dim3(grid), dim3(L::kThreads),
+                  static_cast<size_t>(smem), stream, maps, p);
 }
 
 template <int KIND, int EPI, bool PROMOTE>

@@ -6,8 +6,10 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 #include "gemm_kernel.cuh"
+#include "mxq.h"
 
 namespace mxq {
 
@@ -31,6 +33,28 @@ int64_t option(int32_t which);
 bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                  uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                  CUtensorMapSwizzle swizzle, std::string* err);
+
+// Launch kernel<<<grid, block, smem, stream>>>(args...), with programmatic
+// stream serialization (the kernel may launch while the previous one on
+// the stream finishes; it waits for it in pdl_wait()) unless MXQ_OPT_PDL
+// is 0.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (option(MXQ_OPT_PDL) != 0) {
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 cudaError_t launch_gemm(int kind, int epi, int bt, bool promote, const GemmMaps& maps,
                         const GemmParams& p, int grid, cudaStream_t stream);

@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(1024) moe_align_kernel(const int32_t* __restri
   int* wcnt = run + E;   // [32][E]
   __shared__ int wsum_b[32], wsum_p[32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  pdl_launch_dependents();
 
   for (int i = tid; i < E; i += 1024) {
     cnt[i] = 0;
@@ -166,10 +168,9 @@ cudaError_t launch_moe_align(const int32_t* topk_ids, int64_t S, int32_t E, int3
         cudaFuncSetAttribute(moe_align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  moe_align_kernel<<<1, 1024, smem, stream>>>(topk_ids, static_cast<int>(S), E, block_m,
-                                              static_cast<int>(cap), sorted_ids, expert_ids,
-                                              offsets, num_blocks, status);
-  return cudaGetLastError();
+  return launch_k(moe_align_kernel, dim3(1), dim3(1024), static_cast<size_t>(smem), stream,
+                  topk_ids, static_cast<int>(S), E, block_m, static_cast<int>(cap), sorted_ids,
+                  expert_ids, offsets, num_blocks, status);
 }
 
 // ------------------------------------------------------------ row gather
@@ -181,6 +182,8 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int
                                    const int32_t* __restrict__ offsets,
                                    const int32_t* __restrict__ num_blocks, int BM,
                                    __nv_bfloat16* __restrict__ xs, int vec) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int nb = __ldg(num_blocks);
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -213,10 +216,9 @@ cudaError_t launch_gather_rows(const void* hidden, int64_t ldh, int64_t K, int32
   int64_t blocks = (warps + 7) / 8;
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
-  gather_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(hidden), ldh, K, topk, sorted_ids, offsets,
-      num_blocks, block_m, reinterpret_cast<__nv_bfloat16*>(xs), vec);
-  return cudaGetLastError();
+  return launch_k(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                  reinterpret_cast<const __nv_bfloat16*>(hidden), ldh, K, topk, sorted_ids,
+                  offsets, num_blocks, block_m, reinterpret_cast<__nv_bfloat16*>(xs), vec);
 }
 
 // ------------------------------------------------------------ combine
@@ -224,6 +226,8 @@ cudaError_t launch_gather_rows(const void* hidden, int64_t ldh, int64_t K, int32
 // y already carries the routing weight.
 __global__ void combine_kernel(const float* __restrict__ y, int64_t T, int topk, int64_t K,
                                __nv_bfloat16* __restrict__ out, int64_t ldo, int vec) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   if (vec) {
     const int64_t K4 = K / 4;
@@ -264,9 +268,8 @@ cudaError_t launch_combine(const float* y, int64_t T, int32_t topk, int64_t K, v
   int64_t blocks = (n + 255) / 256;
   if (blocks > 8192) blocks = 8192;
   if (blocks < 1) blocks = 1;
-  combine_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      y, T, topk, K, reinterpret_cast<__nv_bfloat16*>(out), ldo, vec);
-  return cudaGetLastError();
+  return launch_k(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, y, T,
+                  topk, K, reinterpret_cast<__nv_bfloat16*>(out), ldo, vec);
 }
 
 // ------------------------------------------------------ split-K reduction
@@ -274,6 +277,8 @@ cudaError_t launch_combine(const float* y, int64_t T, int32_t topk, int64_t K, v
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int64_t M,
                                      int64_t N, const void* bias, int bias_dtype, void* out,
                                      int out_dtype, int64_t ldo) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < M * N;
        i += stride) {
@@ -297,9 +302,8 @@ cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t M, in
   int64_t blocks = (M * N + 255) / 256;
   if (blocks > 8192) blocks = 8192;
   if (blocks < 1) blocks = 1;
-  splitk_reduce_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      partial, splits, M, N, bias, bias_dtype, out, out_dtype, ldo);
-  return cudaGetLastError();
+  return launch_k(splitk_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                  partial, splits, M, N, bias, bias_dtype, out, out_dtype, ldo);
 }
 
 // ------------------------------------------------------------ debug unsort
@@ -309,6 +313,8 @@ __global__ void unsort_rows_kernel(const __nv_bfloat16* __restrict__ ic1, int64_
                                    const int32_t* __restrict__ offsets,
                                    const int32_t* __restrict__ num_blocks, int BM,
                                    __nv_bfloat16* __restrict__ act_out) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int nb = __ldg(num_blocks);
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -329,10 +335,9 @@ cudaError_t launch_unsort_rows(const void* ic1, int64_t N, const int32_t* sorted
   int64_t blocks = (cap * block_m + 7) / 8;
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
-  unsort_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(ic1), N, sorted_ids, offsets, num_blocks, block_m,
-      reinterpret_cast<__nv_bfloat16*>(act_out));
-  return cudaGetLastError();
+  return launch_k(unsort_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                  reinterpret_cast<const __nv_bfloat16*>(ic1), N, sorted_ids, offsets, num_blocks,
+                  block_m, reinterpret_cast<__nv_bfloat16*>(act_out));
 }
 
 }  // namespace mxq

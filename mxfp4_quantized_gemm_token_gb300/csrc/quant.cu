@@ -37,6 +37,8 @@ __device__ __forceinline__ uint16_t e4m3x2_rn(float lo, float hi) {
 __global__ void group_quant128_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K,
                                       int64_t ldx, float eps, uint8_t* __restrict__ q,
                                       float* __restrict__ scales) {
+  pdl_wait();
+  pdl_launch_dependents();
   constexpr int U = 4;
   const int64_t G = K / 128;
   const int64_t total = M * G;
@@ -101,6 +103,8 @@ __global__ void group_quant128_kernel(const __nv_bfloat16* __restrict__ x, int64
 __global__ void group_quant_generic_kernel(const __nv_bfloat16* __restrict__ x, int64_t M,
                                            int64_t K, int64_t ldx, int group, float eps,
                                            uint8_t* __restrict__ q, float* __restrict__ scales) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t G = (K + group - 1) / group;
   const int64_t total = M * G;
   const int lane = threadIdx.x & 31;
@@ -155,14 +159,12 @@ cudaError_t launch_group_quant(const void* x, int64_t M, int64_t K, int64_t ldx,
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (fast)
-    group_quant128_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
-        reinterpret_cast<const __nv_bfloat16*>(x), M, K, ldx, eps,
-        reinterpret_cast<uint8_t*>(q), scales);
-  else
-    group_quant_generic_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
-        reinterpret_cast<const __nv_bfloat16*>(x), M, K, ldx, group, eps,
-        reinterpret_cast<uint8_t*>(q), scales);
-  return cudaGetLastError();
+    return launch_k(group_quant128_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0,
+                    stream, reinterpret_cast<const __nv_bfloat16*>(x), M, K, ldx, eps,
+                    reinterpret_cast<uint8_t*>(q), scales);
+  return launch_k(group_quant_generic_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0,
+                  stream, reinterpret_cast<const __nv_bfloat16*>(x), M, K, ldx, group, eps,
+                  reinterpret_cast<uint8_t*>(q), scales);
 }
 
 }  // namespace mxq

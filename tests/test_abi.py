@@ -54,6 +54,10 @@ def test_version_and_options_roundtrip(lib):
     assert lib.mxq_set_option(_lib.OPT_FORCE_PATH, 0) == 0
     assert lib.mxq_set_option(_lib.OPT_NORMAL_TILE, 160) == _lib.ERR_INVALID_ARG
     assert b"NORMAL_TILE" in lib.mxq_last_error()
+    assert lib.mxq_get_option(_lib.OPT_PDL, ctypes.byref(v)) == 0 and v.value == 1   # default on
+    assert lib.mxq_set_option(_lib.OPT_PDL, 2) == _lib.ERR_INVALID_ARG
+    assert lib.mxq_set_option(_lib.OPT_PDL, 0) == 0
+    assert lib.mxq_set_option(_lib.OPT_PDL, 1) == 0
 
 
 FAKE = ctypes.c_void_p(1 << 20)   # never dereferenced: validation fails first
