@@ -111,6 +111,19 @@ def test_quant_align_moe_argument_errors(lib):
     sz = ctypes.c_size_t()
     assert lib.mxq_fused_experts_workspace_size(4, 256, 8, 128, 2, 16, 1, ctypes.byref(sz)) == 0
     assert sz.value > 0
+    # block_m 0 is the library's choice: 32 when T*topk <= 16*E, else 64; the
+    # workspace query resolves it the same way the call does
+    def ws(T, topk, E, bm):
+        v = ctypes.c_size_t()
+        assert lib.mxq_fused_experts_workspace_size(T, 7168, E, 2048, topk, bm, 1,
+                                                    ctypes.byref(v)) == 0
+        return v.value
+    assert ws(256, 8, 256, 0) == ws(256, 8, 256, 32)       # 2048 slots <= 16 * 256
+    assert ws(1024, 8, 256, 0) == ws(1024, 8, 256, 64)     # 8192 slots > 16 * 256
+    assert ws(512, 4, 128, 0) == ws(512, 4, 128, 32)       # 2048 = 16 * 128
+    assert ws(1024, 8, 256, 32) != ws(1024, 8, 256, 64)    # the two block sizes differ here
+    assert lib.mxq_fused_experts_workspace_size(4, 256, 8, 128, 2, -1, 1,
+                                                ctypes.byref(sz)) == _lib.ERR_INVALID_ARG
     fe = lib.mxq_fused_experts
     args = [FAKE, 4, 256, 256, 1, 8, 128, FAKE, FAKE, None, FAKE, FAKE, None, FAKE, FAKE, 2, 16,
             FAKE, 256, FAKE, sz.value, None]
