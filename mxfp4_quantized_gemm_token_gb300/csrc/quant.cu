@@ -40,23 +40,35 @@ __global__ void group_quant128_kernel(const __nv_bfloat16* __restrict__ x, int64
   pdl_wait();
   pdl_launch_dependents();
   constexpr int U = 4;
-  const int64_t G = K / 128;
-  const int64_t total = M * G;
+  // the launcher uses this kernel only while M * K/128 < 2^31, so the group
+  // index fits 32 bits: one 32-bit division per iteration locates the row
+  // of the warp's first group, and the others follow by steps (64-bit
+  // division is a long instruction sequence on the GPU)
+  const uint32_t G = static_cast<uint32_t>(K / 128);
+  const uint32_t total = static_cast<uint32_t>(M) * G;
   const int lane = threadIdx.x & 31;
   const int hl = lane & 15;
   const int hw = lane >> 4;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       2 * U * w < total; w += nwarps) {
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (uint32_t w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; 2 * U * w < total;
+       w += nwarps) {
     uint4 raw[U];
     int64_t mm[U], gg[U];
     bool ok[U];
+    const uint32_t base = 2 * U * w;
+    const uint32_t m0 = base / G;
+    const uint32_t r0 = base - m0 * G;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t item = 2 * U * w + 2 * u + hw;
+      const uint32_t item = base + 2 * u + hw;
       ok[u] = item < total;
-      mm[u] = ok[u] ? item / G : 0;
-      gg[u] = ok[u] ? item - mm[u] * G : 0;
+      uint32_t m = m0, r = r0 + 2 * u + hw;
+      while (r >= G) {   // at most once when G >= 8
+        r -= G;
+        ++m;
+      }
+      mm[u] = ok[u] ? m : 0;
+      gg[u] = ok[u] ? r : 0;
       raw[u] = ok[u] ? __ldg(reinterpret_cast<const uint4*>(x + mm[u] * ldx + gg[u] * 128 + hl * 8))
                      : make_uint4(0u, 0u, 0u, 0u);
     }
@@ -137,6 +149,7 @@ cudaError_t launch_group_quant(const void* x, int64_t M, int64_t K, int64_t ldx,
                                float eps, void* q, float* scales, int num_sms,
                                cudaStream_t stream) {
   const bool fast = group == 128 && K % 128 == 0 && ldx % 8 == 0 &&
+                    M * (K / 128) < (int64_t(1) << 31) &&
                     (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
                     (reinterpret_cast<uintptr_t>(q) & 7) == 0;
   const int threads = 256;
