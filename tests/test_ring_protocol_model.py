@@ -63,20 +63,26 @@ class Cta:
     """State and roles of one persistent CTA processing `units` (slice counts)."""
 
     def __init__(self, units, promote, ndg, mxw, AS=12, BS=4, CS=4, SSL=8, NB=4,
-                 old_issuer_rule=False, warps_per_group=2):
+                 old_issuer_rule=False, warps_per_group=2, f8f8=False):
+        # f8f8: FP8 x FP8 (dense and token-major W8A8): one producer loads both
+        # operands of a slice into the A ring, which the MMA issuers read
+        # directly; the scale ring feeds the promotion epilogue; no decode
+        self.f8f8 = f8f8
+        if f8f8:
+            promote, ndg, mxw = True, 0, False
         self.units, self.promote, self.ndg, self.mxw = units, promote, ndg, mxw
         self.AS, self.BS, self.CS, self.SSL, self.NB = AS, BS, CS, SSL, NB
         self.old = old_issuer_rule
         self.wpg = warps_per_group
         W = warps_per_group
         self.a_full = [Bar("a_full%d" % i, 1) for i in range(AS)]
-        self.a_empty = [Bar("a_empty%d" % i, W) for i in range(AS)]
+        self.a_empty = [Bar("a_empty%d" % i, 1 if f8f8 else W) for i in range(AS)]
         self.b_full = [Bar("b_full%d" % i, 1) for i in range(BS)]
         self.b_empty = [Bar("b_empty%d" % i, 1) for i in range(BS)]
         self.c_full = [Bar("c_full%d" % i, W) for i in range(CS)]
         self.c_empty = [Bar("c_empty%d" % i, 1) for i in range(CS)]
         self.s_full = [Bar("s_full%d" % i, 1) for i in range(SSL)]
-        self.s_empty = [Bar("s_empty%d" % i, W) for i in range(SSL)]
+        self.s_empty = [Bar("s_empty%d" % i, 1 if f8f8 else W) for i in range(SSL)]
         self.t_full = [Bar("t_full%d" % i, 1) for i in range(NB)]
         self.t_empty = [Bar("t_empty%d" % i, 1) for i in range(NB)]
         # slot contents: which slice a slot holds, and how far it was consumed
@@ -98,7 +104,8 @@ class Cta:
         for it in range(self.nslices):
             s = it % self.AS
             yield self.a_empty[s], ((it // self.AS) & 1) ^ 1
-            check(it < self.AS or (self.a_slot[s] == it - self.AS and self.a_reads[s] == self.wpg),
+            check(it < self.AS or (self.a_slot[s] == it - self.AS and
+                                   self.a_reads[s] == (1 if self.f8f8 else self.wpg)),
                   "A slot %d refilled for slice %d before slice %s was read by every decode warp"
                   % (s, it, self.a_slot[s]))
 
@@ -123,7 +130,8 @@ class Cta:
         for i in range(self.nslices):
             s = i % self.SSL
             yield self.s_empty[s], ((i // self.SSL) & 1) ^ 1
-            check(i < self.SSL or (self.s_slot[s] == i - self.SSL and self.s_reads[s] == self.wpg),
+            check(i < self.SSL or (self.s_slot[s] == i - self.SSL and
+                                   self.s_reads[s] == (1 if self.f8f8 else self.wpg)),
                   "scale slot %d republished before its slice was read" % s)
             self.s_slot[s], self.s_reads[s] = i, 0
             self.s_full[s].arrive()
@@ -178,6 +186,22 @@ class Cta:
                 buf = au % self.NB if self.promote else ubuf
                 if self.promote:
                     yield self.t_empty[buf], ((au // self.NB) & 1) ^ 1
+                if self.f8f8:
+                    sa = ia % self.AS
+                    yield self.a_full[sa], (ia // self.AS) & 1
+                    check(self.a_slot[sa] == ia, "MMA of slice %d read A slot %d holding slice %s"
+                          % (ia, sa, self.a_slot[sa]))
+
+                    def done(sa=sa, buf=buf, ia=ia):
+                        self.acc[buf] = [ia]
+                        self.a_reads[sa] += 1
+                        self.a_empty[sa].arrive()
+                    self.mma_queue[mine].append(done)
+                    ia += 1
+                    ib += 1
+                    self._commit(mine, self.t_full[buf])
+                    au += 1
+                    continue
                 sa, sb = ia % self.CS, ib % self.BS
                 yield self.c_full[sa], (ia // self.CS) & 1
                 check(all(v == ia for v in self.c_slot[sa]),
@@ -217,6 +241,13 @@ class Cta:
             if self.promote:
                 for k in slices:
                     buf = au % self.NB
+                    if self.f8f8:
+                        ss = k % self.SSL
+                        yield self.s_full[ss], (k // self.SSL) & 1
+                        check(self.s_slot[ss] == k, "epilogue of slice %d read scales of slice %s"
+                              % (k, self.s_slot[ss]))
+                        self.s_reads[ss] += 1
+                        self.s_empty[ss].arrive()
                     yield self.t_full[buf], (au // self.NB) & 1
                     check(self.acc[buf] == [k], "epilogue of slice %d read accumulator %s"
                           % (k, self.acc[buf]))
@@ -243,8 +274,9 @@ class Cta:
     # --------------------------------------------------------- scheduler
     def run(self, rng, max_steps=200000):
         actors = [self.producer_a(), self.issuer(0), self.issuer(1), self.epilogue()]
-        actors.append(self.producer_b())     # every modelled kind has bf16 tokens
-        if self.mxw:
+        if not self.f8f8:
+            actors.append(self.producer_b())     # bf16 tokens
+        if self.mxw or self.f8f8:
             actors.append(self.scale_loader())
         for g in range(self.ndg):
             for w in range(self.wpg):
@@ -318,3 +350,13 @@ def test_model_finds_the_stale_read_of_the_per_unit_issuer_rule():
     # the same schedules are clean with the rule the kernel uses now
     for seed in range(300):
         Cta(UNIT_PATTERNS["odd"], promote=False, ndg=2, mxw=True).run(random.Random(seed))
+
+
+@pytest.mark.parametrize("AS,NB", [(5, 2), (10, 4), (12, 4)])
+@pytest.mark.parametrize("pattern", ["even", "odd", "mixed", "ones"])
+def test_ring_protocol_fp8_x_fp8(AS, NB, pattern):
+    """FP8 x FP8 W8A8: token-major tiles of 192 (5 stages, 2 accumulator
+    buffers) and weight-major decode tiles (10-12 stages, 4 buffers)."""
+    for seed in range(40):
+        cta = Cta(UNIT_PATTERNS[pattern], promote=True, ndg=0, mxw=False, AS=AS, NB=NB, f8f8=True)
+        cta.run(random.Random(seed))
