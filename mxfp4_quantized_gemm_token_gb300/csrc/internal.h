@@ -53,7 +53,11 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  // consume a launch error here (as cudaGetLastError after <<<>>> would), so
+  // that it is reported once, through this library's status
+  if (e != cudaSuccess) (void)cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_gemm(int kind, int epi, int bt, bool promote, const GemmMaps& maps,
