@@ -142,3 +142,24 @@ def test_quant_align_moe_argument_errors(lib):
     bad = list(args)
     bad[1] = 0                                                # no tokens
     assert fe(*bad) == _lib.OK
+
+
+def test_binding_has_no_cpu_fallback():
+    """Every op refuses CPU tensors before touching the library: there is no
+    CPU path behind the binding (the oracle is test infrastructure only)."""
+    import torch
+    import mxfp4_quantized_gemm_token_gb300 as mxq
+    x = torch.zeros(4, 256, dtype=torch.bfloat16)
+    w = torch.zeros(128, 256, dtype=torch.uint8).view(torch.float8_e4m3fn)
+    ws = torch.ones(1, 2)
+    with pytest.raises(ValueError, match="CUDA"):
+        mxq.per_token_group_quant_fp8(x)
+    with pytest.raises(ValueError, match="CUDA"):
+        mxq.fp8_scaled_mm(x, w, torch.ones(()), None)
+    with pytest.raises(ValueError, match="CUDA"):
+        mxq.moe_align_block(torch.zeros(4, 2, dtype=torch.int32), 8, 16)
+    w1 = torch.zeros(2, 256, 256, dtype=torch.uint8).view(torch.float8_e4m3fn)
+    with pytest.raises(ValueError, match="CUDA"):
+        mxq.fused_experts(x, w1, ws, w1, ws, torch.ones(4, 1), torch.zeros(4, 1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="block sizes"):
+        mxq.w8a8_block_fp8_linear(x, w, [1, 32], ws)      # MXFP8-style [1, 32] blocks
