@@ -71,6 +71,9 @@ class Cta:
         if f8f8:
             promote, ndg, mxw = True, 0, False
         self.units, self.promote, self.ndg, self.mxw = units, promote, ndg, mxw
+        # the scale ring feeds the decode (MXFP4) or the promotion epilogue
+        # (promoted kinds); per-tensor whole-K has none
+        self.epi_scales = promote
         self.AS, self.BS, self.CS, self.SSL, self.NB = AS, BS, CS, SSL, NB
         self.old = old_issuer_rule
         self.wpg = warps_per_group
@@ -82,7 +85,7 @@ class Cta:
         self.c_full = [Bar("c_full%d" % i, W) for i in range(CS)]
         self.c_empty = [Bar("c_empty%d" % i, 1) for i in range(CS)]
         self.s_full = [Bar("s_full%d" % i, 1) for i in range(SSL)]
-        self.s_empty = [Bar("s_empty%d" % i, 1 if f8f8 else W) for i in range(SSL)]
+        self.s_empty = [Bar("s_empty%d" % i, 1 if promote else W) for i in range(SSL)]
         self.t_full = [Bar("t_full%d" % i, 1) for i in range(NB)]
         self.t_empty = [Bar("t_empty%d" % i, 1) for i in range(NB)]
         # slot contents: which slice a slot holds, and how far it was consumed
@@ -131,7 +134,7 @@ class Cta:
             s = i % self.SSL
             yield self.s_empty[s], ((i // self.SSL) & 1) ^ 1
             check(i < self.SSL or (self.s_slot[s] == i - self.SSL and
-                                   self.s_reads[s] == (1 if self.f8f8 else self.wpg)),
+                                   self.s_reads[s] == (1 if self.epi_scales else self.wpg)),
                   "scale slot %d republished before its slice was read" % s)
             self.s_slot[s], self.s_reads[s] = i, 0
             self.s_full[s].arrive()
@@ -241,7 +244,7 @@ class Cta:
             if self.promote:
                 for k in slices:
                     buf = au % self.NB
-                    if self.f8f8:
+                    if self.epi_scales:
                         ss = k % self.SSL
                         yield self.s_full[ss], (k // self.SSL) & 1
                         check(self.s_slot[ss] == k, "epilogue of slice %d read scales of slice %s"
@@ -276,7 +279,7 @@ class Cta:
         actors = [self.producer_a(), self.issuer(0), self.issuer(1), self.epilogue()]
         if not self.f8f8:
             actors.append(self.producer_b())     # bf16 tokens
-        if self.mxw or self.f8f8:
+        if self.mxw or self.epi_scales:
             actors.append(self.scale_loader())
         for g in range(self.ndg):
             for w in range(self.wpg):
