@@ -10,7 +10,7 @@ reads its own copy of W (6 distinct 132 MB copies), so no GEMM finds its
 weights in the 129 MB L2.
 
 Other workloads (--workload) measure the remaining hot-path configurations
-for the tables in the design doc; the default line is the contract line.
+for the results tables; the default line is the contract line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """

@@ -21,7 +21,7 @@
  *                 BlockWise128x128 / 1x128 weights) and the numerical test
  *                 (reference_block_fp8_matmul = dequantise, then matmul).
  *
- * Readings where the pages are silent (each is also listed in the design doc):
+ * Readings where the pages are silent:
  *   - group scale s = max(amax, eps) / 448 in fp32 with IEEE division, and
  *     q = e4m3_rne(clamp(x / s, -448, 448)) with IEEE fp32 division;
  *   - e4m3 encode = nearest finite code, ties to the even code, sign kept
