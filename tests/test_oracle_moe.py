@@ -217,3 +217,51 @@ def test_expert_permutation_invariance_and_weight_linearity(oracle):
     twice = oracle.fused_experts(bits(x), W_FP8, u8(w1), s1.numpy(), None, u8(w2), s2.numpy(),
                                  None, (2 * tw).numpy(), ids.numpy(), N)
     assert torch.equal(bf16_of(twice).float(), 2 * bf16_of(base).float())
+
+
+@pytest.mark.parametrize("wtype,topk,E", [(W_FP8, 2, 3), (W_MX, 2, 4), (W_FP8, 8, 10),
+                                          (W_MX, 8, 9)])
+def test_topk_combine_matches_weighted_dense_mlps(oracle, wtype, topk, E):
+    """topk > 1 with deliberately unequal routing weights: every checkpoint row
+    at slot t*topk + k must be the dense MLP of token t through expert
+    ids[t, k], and the output must be sum_k w[t, k] * z_(t,k) in ascending k.
+    The reference is built from library fp64 matmuls of independently
+    dequantised weights, so a transposed weight index (w[k*T + t]) or a
+    token-major / expert-major slot mix-up in act or z fails it."""
+    N, K, T = 128, 256, 5
+    if wtype == W_FP8:
+        w1, s1, w2, s2 = synth.moe_fp8_weights(E, N, K, seed=31)
+        W1, W2 = deq_fp8(w1, s1), deq_fp8(w2, s2)
+        b1 = b2 = None
+        sc = lambda s: s.numpy()
+    else:
+        w1, s1, w2, s2 = synth.moe_mxfp4_weights(E, N, K, seed=31)
+        W1, W2 = deq_mx(w1, s1), deq_mx(w2, s2)
+        b1, b2 = synth.moe_biases(E, N, K, seed=32)
+        sc = u8
+    x = synth.activations(T, K, seed=33, scale_div=10)
+    g = torch.Generator().manual_seed(34)
+    ids = torch.stack([torch.randperm(E, generator=g)[:topk] for _ in range(T)]).to(torch.int32)
+    base = (torch.tensor([0.7, 0.2, 0.1]) if topk == 2 else
+            torch.tensor([0.31, 0.22, 0.15, 0.11, 0.09, 0.07, 0.04, 0.01]))
+    tw = torch.stack([base[torch.randperm(base.numel(), generator=g)][:topk] * (1 + 0.5 * t)
+                      for t in range(T)]).float()
+    out, act, z = oracle.fused_experts(
+        bits(x), wtype, u8(w1), sc(s1), None if b1 is None else b1.numpy(), u8(w2), sc(s2),
+        None if b2 is None else b2.numpy(), tw.numpy(), ids.numpy(), N, checkpoints=True)
+    for t in range(T):
+        o = torch.zeros(K, dtype=torch.float64)
+        for k in range(topk):
+            e, slot = int(ids[t, k]), t * topk + k
+            ra, _ = dense_mlp(x[t:t + 1], W1[e], None if b1 is None else b1[e], W2[e],
+                              None if b2 is None else b2[e], N)
+            ga = bf16_of(act[slot]).double()
+            # act: one bf16 step of freedom where the fp64 summation order
+            # lands on the other side of a rounding boundary
+            assert torch.allclose(ga, ra.double()[0], rtol=2 ** -7, atol=1e-6), (t, k)
+            # z from the oracle's own act row: only summation order differs
+            rz = ga @ W2[e].T + (0 if b2 is None else b2[e].double())
+            assert np.allclose(z[slot], rz.numpy(), rtol=1e-9, atol=1e-12), (t, k)
+            o += float(tw[t, k]) * rz
+        ref = o.float().to(torch.bfloat16).float()
+        assert torch.equal(bf16_of(out[t]).float(), ref), t
