@@ -232,7 +232,8 @@ def run_gpu(args, world, rank, local):
     lib = mxq._lib.load()
     for M in M_SET:
         sz = ctypes.c_size_t(0)
-        mxq.check(lib.mxq_fp8_scaled_mm_workspace_size(M, N_W, K_W, 3, ctypes.byref(sz)))
+        mxq.check(lib.mxq_fp8_scaled_mm_workspace_size(M, N_W, K_W, 3, 128, 128,
+                                                            ctypes.byref(sz)))
         workspaces.append(torch.empty(sz.value, dtype=torch.uint8, device=dev) if sz.value else None)
         launches_per_step += 2 + (1 if sz.value else 0)
     torch.cuda.synchronize()

@@ -133,8 +133,10 @@ mxq_status mxq_per_token_group_quant_fp8(const void* x, int64_t M, int64_t K, in
  *   bias   NULL, or [N] of bias_dtype MXQ_F32 / MXQ_BF16
  *   out    [M, N] row stride ldo; out_dtype MXQ_BF16 (rounded to nearest even
  *          from the fp32 accumulator) or MXQ_F32 (the accumulator itself)
- *   workspace / ws_bytes: optional device scratch for split-K (see
- *          mxq_fp8_scaled_mm_workspace_size); NULL/0 disables split-K.
+ *   workspace / ws_bytes: device scratch for split-K, 16-byte aligned, of
+ *          at least mxq_fp8_scaled_mm_workspace_size bytes for the same
+ *          arguments (a smaller non-NULL workspace is MXQ_ERR_INVALID_ARG);
+ *          NULL runs the same GEMM without split-K.
  * Block sizes other than [128,128], [1,128] and per-tensor (e.g. MXFP8
  * [1, 32]) give MXQ_ERR_UNSUPPORTED, as the page's block_size check does.
  * M == 0 or N == 0 is a no-op; K must be positive.
@@ -160,9 +162,10 @@ mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t M, int64_t 
  *   - A shape whose split-K plan needs more scratch than that is rejected with
  *     MXQ_ERR_UNSUPPORTED (mxq_last_error says how much it needs); shapes that
  *     need no split (large M) need no scratch and are always accepted.
- *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before any
- *     stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (a host-side query, no allocation); the set-up is therefore the same
+ *     on every call, and a first call before any stream capture is advised
+ *     only because the library loads its kernels then.
  *   - Every call on a device shares the one array and its contents are left
  *     from the previous call (the partials are fully rewritten, so nothing
  *     needs to start at zero).  Calls whose executions overlap on the GPU,
@@ -176,10 +179,13 @@ mxq_status mxq_fp8_scaled_mm_noalloc(const void* A, int32_t a_dtype, int64_t M, 
                                      const void* bias, int32_t bias_dtype, void* out,
                                      int32_t out_dtype, int64_t ldo, mxq_stream_t stream);
 
-/* Workspace bytes that let mxq_fp8_scaled_mm use its preferred split-K plan
- * for this shape on the current device (0 when no split is needed). */
+/* Workspace bytes of the split-K plan mxq_fp8_scaled_mm runs for this shape
+ * on the current device (0 when it does not split).  The plan depends on the
+ * activation type and the weight block size (a_dtype, block_n, block_k take
+ * the values the call will get), so the size describes exactly that call.
+ * Unsupported block sizes give MXQ_ERR_UNSUPPORTED as in the call. */
 mxq_status mxq_fp8_scaled_mm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t a_dtype,
-                                            size_t* bytes);
+                                            int32_t block_n, int32_t block_k, size_t* bytes);
 
 /*
  * Expert-block alignment ([CPU-MoE], the stage-1 tile loop consumes
@@ -235,9 +241,11 @@ mxq_status mxq_fused_experts(const void* hidden, int64_t T, int64_t K, int64_t l
                              const int32_t* topk_ids, int32_t topk, int32_t block_m, void* out,
                              int64_t ldo, void* workspace, size_t ws_bytes, mxq_stream_t stream);
 
-/* Same as mxq_fused_experts, and additionally copies the checkpoints in slot
- * order (slot = t*topk + k): act_out bf16 [T*topk, N] and y_out fp32
- * [T*topk, K] = topk_weight * z.  Either may be NULL. */
+/* Same as mxq_fused_experts, and additionally writes the checkpoints in slot
+ * order (slot = t*topk + k): act_out bf16 [T*topk, N], y_out fp32
+ * [T*topk, K] = topk_weight * z, and h_out fp32 [T*topk, 2N] = the stage-1
+ * accumulator hidden . W1[e]^T before the bias (gate rows first).  Any of
+ * them may be NULL. */
 mxq_status mxq_fused_experts_debug(const void* hidden, int64_t T, int64_t K, int64_t ldh,
                                    int32_t wtype, int32_t E, int64_t N, const void* w1,
                                    const void* w1_scale, const float* w1_bias, const void* w2,
@@ -245,7 +253,7 @@ mxq_status mxq_fused_experts_debug(const void* hidden, int64_t T, int64_t K, int
                                    const float* topk_weights, const int32_t* topk_ids,
                                    int32_t topk, int32_t block_m, void* out, int64_t ldo,
                                    void* workspace, size_t ws_bytes, void* act_out,
-                                   float* y_out, mxq_stream_t stream);
+                                   float* y_out, float* h_out, mxq_stream_t stream);
 
 mxq_status mxq_fused_experts_workspace_size(int64_t T, int64_t K, int32_t E, int64_t N,
                                             int32_t topk, int32_t block_m, int32_t wtype,

@@ -104,6 +104,9 @@ def fp8_scaled_mm(a, w, w_scale, block_size=None, a_scale=None, bias=None,
     [..., K] with a_scale None (W8A16); w: e4m3 [N, K]; w_scale: fp32 0-d/[1]
     (per-tensor, block_size None) or [ceil(N/bn), ceil(K/128)] with
     block_size [bn, 128], bn in {1, 128}, any strides.
+    workspace: None (the library's split-K plan, sized by the workspace
+    query and allocated here) or a caller buffer of at least that size; an
+    empty buffer runs without split-K.
     """
     _need_cuda(a, w, w_scale, a_scale, bias)
     lib = _lib_handle()
@@ -146,7 +149,7 @@ def fp8_scaled_mm(a, w, w_scale, block_size=None, a_scale=None, bias=None,
     ws_bytes = 0
     if workspace is None:
         sz = ctypes.c_size_t(0)
-        check(lib.mxq_fp8_scaled_mm_workspace_size(M, N, K, a_dtype, ctypes.byref(sz)))
+        check(lib.mxq_fp8_scaled_mm_workspace_size(M, N, K, a_dtype, bn, bk, ctypes.byref(sz)))
         if sz.value:
             workspace = torch.empty(sz.value, dtype=torch.uint8, device=a.device)
     if workspace is not None:
@@ -154,7 +157,7 @@ def fp8_scaled_mm(a, w, w_scale, block_size=None, a_scale=None, bias=None,
     check(lib.mxq_fp8_scaled_mm(
         _ptr(a2), a_dtype, M, K, a2.stride(0), _ptr(a_scale), sa0, sa1, _ptr(w), N, w.stride(0),
         _ptr(w_scale), bn, bk, sw0, sw1, _ptr(bias), bias_dtype, _ptr(out), od, N,
-        _ptr(workspace), ws_bytes, _stream(a.device)))
+        _ptr(workspace) if ws_bytes else None, ws_bytes, _stream(a.device)))
     return out.view(*a.shape[:-1], N)
 
 
@@ -212,7 +215,10 @@ def fused_experts(hidden, w1, w1_scale, w2, w2_scale, topk_weights, topk_ids,
     """Routed MoE: align, stage 1 (+ SiLU-and-mul), stage 2, top-k combine.
 
     block_m: tokens per expert block (16, 32, 64, 128), or 0 for the
-    library's choice (32 when T*topk <= 16*E, else 64)."""
+    library's choice (32 when T*topk <= 16*E, else 64).
+    checkpoints: also return, in slot order (t*topk + k), act (bf16 [S, N]),
+    y = w * z (fp32 [S, K]) and the stage-1 accumulator h before the bias
+    (fp32 [S, 2N])."""
     _need_cuda(hidden, w1, w1_scale, w2, w2_scale, topk_weights, topk_ids, w1_bias, w2_bias)
     lib = _lib_handle()
     T, K = hidden.shape
@@ -238,7 +244,9 @@ def fused_experts(hidden, w1, w1_scale, w2, w2_scale, topk_weights, topk_ids,
     if checkpoints:
         act = torch.empty((T * topk, N), dtype=torch.bfloat16, device=hidden.device)
         y = torch.empty((T * topk, K), dtype=torch.float32, device=hidden.device)
-        check(lib.mxq_fused_experts_debug(*args, _ptr(act), _ptr(y), _stream(hidden.device)))
-        return out, act, y
+        h = torch.empty((T * topk, 2 * N), dtype=torch.float32, device=hidden.device)
+        check(lib.mxq_fused_experts_debug(*args, _ptr(act), _ptr(y), _ptr(h),
+                                          _stream(hidden.device)))
+        return out, act, y, h
     check(lib.mxq_fused_experts(*args, _stream(hidden.device)))
     return out

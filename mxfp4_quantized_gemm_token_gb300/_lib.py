@@ -53,12 +53,13 @@ def _declare(lib):
                                    I64, I64, P, I32, P, I32, I64, P, SZ, P]),
         "mxq_fp8_scaled_mm_noalloc": (st, [P, I32, I64, I64, I64, P, I64, I64, P, I64, I64, P,
                                            I32, I32, I64, I64, P, I32, P, I32, I64, P]),
-        "mxq_fp8_scaled_mm_workspace_size": (st, [I64, I64, I64, I32, ctypes.POINTER(SZ)]),
+        "mxq_fp8_scaled_mm_workspace_size": (st, [I64, I64, I64, I32, I32, I32,
+                                                  ctypes.POINTER(SZ)]),
         "mxq_moe_align_block": (st, [P, I64, I32, I32, I32, P, P, P, P, I64, P, SZ, P]),
         "mxq_fused_experts": (st, [P, I64, I64, I64, I32, I32, I64, P, P, P, P, P, P, P, P, I32,
                                    I32, P, I64, P, SZ, P]),
         "mxq_fused_experts_debug": (st, [P, I64, I64, I64, I32, I32, I64, P, P, P, P, P, P, P, P,
-                                         I32, I32, P, I64, P, SZ, P, P, P]),
+                                         I32, I32, P, I64, P, SZ, P, P, P, P]),
         "mxq_fused_experts_workspace_size": (st, [I64, I64, I32, I64, I32, I32, I32,
                                                   ctypes.POINTER(SZ)]),
     }

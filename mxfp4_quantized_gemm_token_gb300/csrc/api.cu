@@ -79,15 +79,18 @@ bool device_info(DeviceInfo* info, std::string* err) {
              std::to_string(n.cc_major) + "." + std::to_string(n.cc_minor);
       return false;
     }
-    void* p = nullptr;
-    if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) {
-      *err = std::string("cudaGetSymbolAddress(status): ") + cudaGetErrorString(e);
-      return false;
-    }
-    n.status = reinterpret_cast<int*>(p);
     d = n;
   }
   *info = d;
+  // The status word's device address is looked up on every call (a cheap
+  // host-side query) rather than cached, so a reset device or another
+  // context on it never receives a stale address.
+  void* p = nullptr;
+  if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) {
+    *err = std::string("cudaGetSymbolAddress(status): ") + cudaGetErrorString(e);
+    return false;
+  }
+  info->status = reinterpret_cast<int*>(p);
   return true;
 }
 
@@ -256,30 +259,16 @@ int sms_for_grid(const DeviceInfo& d) {
 
 }  // namespace
 
-extern "C" mxq_status mxq_fp8_scaled_mm_workspace_size(int64_t M, int64_t N, int64_t K,
-                                                       int32_t a_dtype, size_t* bytes) {
-  if (!bytes || M < 0 || N < 0 || K <= 0)
-    return fail(MXQ_ERR_INVALID_ARG, "bad sizes or NULL result pointer");
-  DeviceInfo d;
-  std::string err;
-  if (!device_info(&d, &err)) return fail(MXQ_ERR_UNSUPPORTED, err);
-  if (M == 0 || N == 0) {
-    *bytes = 0;
-    return MXQ_OK;
-  }
-  const MmPlan pl = plan_mm(M, N, K, a_dtype, true, a_dtype == MXQ_E4M3, sms_for_grid(d));
-  *bytes = pl.splits > 1 ? static_cast<size_t>(pl.splits) * M * N * sizeof(float) : 0;
-  return MXQ_OK;
-}
+namespace mxq {
 
-extern "C" mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t M, int64_t K,
-                                        int64_t lda, const float* a_scale, int64_t sa0,
-                                        int64_t sa1, const void* W, int64_t N, int64_t ldw,
-                                        const float* w_scale, int32_t block_n, int32_t block_k,
-                                        int64_t sw0, int64_t sw1, const void* bias,
-                                        int32_t bias_dtype, void* out, int32_t out_dtype,
-                                        int64_t ldo, void* workspace, size_t ws_bytes,
-                                        mxq_stream_t stream) {
+// Host-side argument checks of mxq_fp8_scaled_mm (and its no-alloc variant):
+// MXQ_OK, or the status and message of the first problem found.  Sizes with
+// M == 0 or N == 0 pass (the call is then a no-op).
+mxq_status validate_mm(const void* A, int32_t a_dtype, int64_t M, int64_t K, int64_t lda,
+                       const float* a_scale, int64_t sa0, int64_t sa1, const void* W, int64_t N,
+                       int64_t ldw, const float* w_scale, int32_t block_n, int32_t block_k,
+                       int64_t sw0, int64_t sw1, const void* bias, int32_t bias_dtype,
+                       const void* out, int32_t out_dtype, int64_t ldo) {
   if (M < 0 || N < 0 || K <= 0) return fail(MXQ_ERR_INVALID_ARG, "need M, N >= 0 and K > 0");
   if (M == 0 || N == 0) return MXQ_OK;
   if (!A || !W || !out || !w_scale)
@@ -310,16 +299,90 @@ extern "C" mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t 
                 "A and W need 16-byte aligned bases and row strides that are multiples of 16 bytes");
   if (block && (sw0 < 0 || sw1 < 0 || (a_scale && (sa0 < 0 || sa1 < 0))))
     return fail(MXQ_ERR_INVALID_ARG, "negative scale strides");
+  return MXQ_OK;
+}
+
+}  // namespace mxq
+
+namespace {
+
+// The plan mxq_fp8_scaled_mm runs for a validated argument set.  The
+// workspace query and the no-alloc entry point use the same function, so the
+// size they report is the size of the split the call actually makes.
+MmPlan plan_for_call(int64_t M, int64_t N, int64_t K, int32_t a_dtype, int32_t block_n,
+                     int32_t block_k, int sms) {
+  const bool block = !(block_n == 0 && block_k == 0);
+  return plan_mm(M, N, K, a_dtype, block, a_dtype == MXQ_E4M3, sms, block_n != 1);
+}
+
+size_t plan_workspace_bytes(const MmPlan& pl, int64_t M, int64_t N) {
+  return pl.splits > 1 ? static_cast<size_t>(pl.splits) * M * N * sizeof(float) : 0;
+}
+
+}  // namespace
+
+namespace mxq {
+
+mxq_status mm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t a_dtype, int32_t block_n,
+                              int32_t block_k, size_t* bytes) {
+  *bytes = 0;
+  if (M == 0 || N == 0) return MXQ_OK;
+  DeviceInfo d;
+  std::string err;
+  if (!device_info(&d, &err)) return fail(MXQ_ERR_UNSUPPORTED, err);
+  *bytes = plan_workspace_bytes(plan_for_call(M, N, K, a_dtype, block_n, block_k, sms_for_grid(d)),
+                                M, N);
+  return MXQ_OK;
+}
+
+}  // namespace mxq
+
+extern "C" mxq_status mxq_fp8_scaled_mm_workspace_size(int64_t M, int64_t N, int64_t K,
+                                                       int32_t a_dtype, int32_t block_n,
+                                                       int32_t block_k, size_t* bytes) {
+  if (!bytes || M < 0 || N < 0 || K <= 0)
+    return fail(MXQ_ERR_INVALID_ARG, "bad sizes or NULL result pointer");
+  if (a_dtype != MXQ_E4M3 && a_dtype != MXQ_BF16)
+    return fail(MXQ_ERR_UNSUPPORTED, "a_dtype must be MXQ_E4M3 (W8A8) or MXQ_BF16 (W8A16)");
+  if (!(block_n == 0 && block_k == 0) && !(block_k == 128 && (block_n == 1 || block_n == 128)))
+    return fail(MXQ_ERR_UNSUPPORTED,
+                "weight block size must be [128, 128], [1, 128] or per-tensor [0, 0]");
+  return mm_workspace_bytes(M, N, K, a_dtype, block_n, block_k, bytes);
+}
+
+extern "C" mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t M, int64_t K,
+                                        int64_t lda, const float* a_scale, int64_t sa0,
+                                        int64_t sa1, const void* W, int64_t N, int64_t ldw,
+                                        const float* w_scale, int32_t block_n, int32_t block_k,
+                                        int64_t sw0, int64_t sw1, const void* bias,
+                                        int32_t bias_dtype, void* out, int32_t out_dtype,
+                                        int64_t ldo, void* workspace, size_t ws_bytes,
+                                        mxq_stream_t stream) {
+  const mxq_status vst = validate_mm(A, a_dtype, M, K, lda, a_scale, sa0, sa1, W, N, ldw, w_scale,
+                                     block_n, block_k, sw0, sw1, bias, bias_dtype, out, out_dtype,
+                                     ldo);
+  if (vst != MXQ_OK) return vst;
+  if (M == 0 || N == 0) return MXQ_OK;
+  const bool per_tensor = block_n == 0 && block_k == 0;
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 15) != 0)
+    return fail(MXQ_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   DeviceInfo d;
   std::string err;
   if (!device_info(&d, &err)) return fail(MXQ_ERR_UNSUPPORTED, err);
   const int sms = sms_for_grid(d);
-  MmPlan pl = plan_mm(M, N, K, a_dtype, block, a_scale != nullptr, sms, block_n != 1);
-  if (pl.splits > 1 &&
-      (workspace == nullptr || ws_bytes < static_cast<size_t>(pl.splits) * M * N * sizeof(float) ||
-       (reinterpret_cast<uintptr_t>(workspace) & 15) != 0)) {
-    pl.splits = 1;
-    pl.kb_per_split = pl.nkb;
+  MmPlan pl = plan_for_call(M, N, K, a_dtype, block_n, block_k, sms);
+  const size_t need = plan_workspace_bytes(pl, M, N);
+  if (need > 0) {
+    if (workspace == nullptr) {
+      // no workspace: the same GEMM without split-K
+      pl.splits = 1;
+      pl.kb_per_split = pl.nkb;
+    } else if (ws_bytes < need) {
+      return fail(MXQ_ERR_INVALID_ARG,
+                  "workspace of " + std::to_string(ws_bytes) + " bytes is smaller than the " +
+                      std::to_string(need) +
+                      " this shape's split-K plan needs (mxq_fp8_scaled_mm_workspace_size)");
+    }
   }
 
   GemmMaps maps;
@@ -473,7 +536,7 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
                               const float* w2_bias, const float* topk_weights,
                               const int32_t* topk_ids, int32_t topk, int32_t block_m, void* out,
                               int64_t ldo, void* workspace, size_t ws_bytes, void* act_out,
-                              float* y_out, cudaStream_t st) {
+                              float* y_out, float* h_out, cudaStream_t st) {
   if (T < 0 || K <= 0 || N <= 0 || topk <= 0)
     return fail(MXQ_ERR_INVALID_ARG, "need T >= 0, K > 0, N > 0, topk > 0");
   if (T == 0) return MXQ_OK;
@@ -603,6 +666,7 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
     p.bias_dtype = MXQ_F32;
     p.bias_e = rows;
     p.route_w = topk_weights;
+    p.h_out = stage == 0 ? h_out : nullptr;
     p.out = stage == 0 ? ic1 : static_cast<void*>(y);
     p.out_dtype = stage == 0 ? MXQ_BF16 : MXQ_F32;
     p.ldo = stage == 0 ? N : K;
@@ -648,7 +712,8 @@ extern "C" mxq_status mxq_fused_experts(const void* hidden, int64_t T, int64_t K
                                         void* workspace, size_t ws_bytes, mxq_stream_t stream) {
   return fused_experts_impl(hidden, T, K, ldh, wtype, E, N, w1, w1_scale, w1_bias, w2, w2_scale,
                             w2_bias, topk_weights, topk_ids, topk, block_m, out, ldo, workspace,
-                            ws_bytes, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+                            ws_bytes, nullptr, nullptr, nullptr,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" mxq_status mxq_fused_experts_debug(
@@ -656,8 +721,8 @@ extern "C" mxq_status mxq_fused_experts_debug(
     const void* w1, const void* w1_scale, const float* w1_bias, const void* w2,
     const void* w2_scale, const float* w2_bias, const float* topk_weights, const int32_t* topk_ids,
     int32_t topk, int32_t block_m, void* out, int64_t ldo, void* workspace, size_t ws_bytes,
-    void* act_out, float* y_out, mxq_stream_t stream) {
+    void* act_out, float* y_out, float* h_out, mxq_stream_t stream) {
   return fused_experts_impl(hidden, T, K, ldh, wtype, E, N, w1, w1_scale, w1_bias, w2, w2_scale,
                             w2_bias, topk_weights, topk_ids, topk, block_m, out, ldo, workspace,
-                            ws_bytes, act_out, y_out, reinterpret_cast<cudaStream_t>(stream));
+                            ws_bytes, act_out, y_out, h_out, reinterpret_cast<cudaStream_t>(stream));
 }

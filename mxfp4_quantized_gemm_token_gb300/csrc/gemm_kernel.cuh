@@ -98,6 +98,7 @@ struct GemmParams {
   int bias_dtype;
   int64_t bias_e;
   const float* route_w;
+  float* h_out;       // SiLU stage, debug: the fp32 accumulator (before bias) in slot order, or NULL
   void* out;
   int out_dtype;
   int64_t ldo;
@@ -1139,6 +1140,12 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
                 const int col = col0 + c * STG + jj;
                 if (col >= U.rows) break;
                 if (ok) {
+                  if (p.h_out != nullptr) {
+                    const int64_t hs = __ldg(p.sorted_ids + static_cast<int64_t>(U.blk) * p.block_m + col);
+                    float* hr = p.h_out + hs * (2 * static_cast<int64_t>(p.n_half));
+                    hr[U.n0 + l] = stg[jj * 128 + l];
+                    hr[p.n_half + U.n0 + l] = stg[jj * 128 + 64 + l];
+                  }
                   const float gt = stg[jj * 128 + l] + bias_g;
                   const float up = stg[jj * 128 + 64 + l] + bias_u;
                   const float a = gt / (1.0f + expf(-gt)) * up;

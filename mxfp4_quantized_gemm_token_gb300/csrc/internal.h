@@ -29,6 +29,19 @@ void set_last_error(const std::string& msg);
 // Process-wide options (see MXQ_OPT_*).
 int64_t option(int32_t which);
 
+// Host-side argument checks of mxq_fp8_scaled_mm: MXQ_OK or the first
+// problem's status (with mxq_last_error set).
+mxq_status validate_mm(const void* A, int32_t a_dtype, int64_t M, int64_t K, int64_t lda,
+                       const float* a_scale, int64_t sa0, int64_t sa1, const void* W, int64_t N,
+                       int64_t ldw, const float* w_scale, int32_t block_n, int32_t block_k,
+                       int64_t sw0, int64_t sw1, const void* bias, int32_t bias_dtype,
+                       const void* out, int32_t out_dtype, int64_t ldo);
+
+// Split-K scratch bytes of the plan mxq_fp8_scaled_mm runs for these sizes
+// on the current device (0: no split).
+mxq_status mm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t a_dtype, int32_t block_n,
+                              int32_t block_k, size_t* bytes);
+
 // tensor-map encode through the driver entry point (no libcuda link)
 bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                  uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,

@@ -10,7 +10,6 @@
 // itself, so a call needs nothing but its inputs and outputs.
 #include <cuda_runtime.h>
 
-#include <mutex>
 #include <string>
 
 #include "internal.h"
@@ -22,9 +21,6 @@ namespace {
 // exits.  MXQ_NOALLOC_SCRATCH_BYTES is its size.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MXQ_NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_mu;
-void* g_scratch_ptr[64] = {nullptr};
-
 }  // namespace
 
 extern "C" mxq_status mxq_fp8_scaled_mm_noalloc(
@@ -32,14 +28,15 @@ extern "C" mxq_status mxq_fp8_scaled_mm_noalloc(
     int64_t sa0, int64_t sa1, const void* W, int64_t N, int64_t ldw, const float* w_scale,
     int32_t block_n, int32_t block_k, int64_t sw0, int64_t sw1, const void* bias,
     int32_t bias_dtype, void* out, int32_t out_dtype, int64_t ldo, mxq_stream_t stream) {
-  if (M < 0 || N < 0 || K <= 0) return mxq_fp8_scaled_mm(A, a_dtype, M, K, lda, a_scale, sa0, sa1,
-                                                         W, N, ldw, w_scale, block_n, block_k, sw0,
-                                                         sw1, bias, bias_dtype, out, out_dtype,
-                                                         ldo, nullptr, 0, stream);
+  // the arguments first, so a bad call reports its real error
+  const mxq_status vst =
+      mxq::validate_mm(A, a_dtype, M, K, lda, a_scale, sa0, sa1, W, N, ldw, w_scale, block_n,
+                       block_k, sw0, sw1, bias, bias_dtype, out, out_dtype, ldo);
+  if (vst != MXQ_OK) return vst;
   if (M == 0 || N == 0) return MXQ_OK;
-  // the split-K partials this shape needs on this device
+  // the split-K partials of the plan the call will run on this device
   size_t need = 0;
-  mxq_status st = mxq_fp8_scaled_mm_workspace_size(M, N, K, a_dtype, &need);
+  const mxq_status st = mxq::mm_workspace_bytes(M, N, K, a_dtype, block_n, block_k, &need);
   if (st != MXQ_OK) return st;
   if (need > static_cast<size_t>(MXQ_NOALLOC_SCRATCH_BYTES)) {
     mxq::set_last_error("mxq_fp8_scaled_mm_noalloc: this shape needs " + std::to_string(need) +
@@ -48,30 +45,21 @@ extern "C" mxq_status mxq_fp8_scaled_mm_noalloc(
                         " bytes; use mxq_fp8_scaled_mm with a workspace");
     return MXQ_ERR_UNSUPPORTED;
   }
-  // set-up once per device, with that device current: the device address of
-  // the array (its host-side name is only a stand-in)
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    mxq::set_last_error("mxq_fp8_scaled_mm_noalloc: no current CUDA device");
-    return MXQ_ERR_CUDA;
-  }
   void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
-      void* p = nullptr;
-      const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-      if (e != cudaSuccess) {
-        mxq::set_last_error(std::string("mxq_fp8_scaled_mm_noalloc: cudaGetSymbolAddress: ") +
-                            cudaGetErrorString(e));
-        return MXQ_ERR_CUDA;
-      }
-      g_scratch_ptr[dev] = p;
+  if (need > 0) {
+    // The array's name in host code is only a stand-in; its device address
+    // on the current device is looked up on every call (a cheap host-side
+    // query), so a reset device or a different context never sees a stale
+    // address.
+    const cudaError_t e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      mxq::set_last_error(std::string("mxq_fp8_scaled_mm_noalloc: cudaGetSymbolAddress: ") +
+                          cudaGetErrorString(e));
+      return MXQ_ERR_CUDA;
     }
-    scratch = g_scratch_ptr[dev];
   }
   // The partials are fully rewritten by every split, so nothing needs clearing.
   return mxq_fp8_scaled_mm(A, a_dtype, M, K, lda, a_scale, sa0, sa1, W, N, ldw, w_scale, block_n,
                            block_k, sw0, sw1, bias, bias_dtype, out, out_dtype, ldo, scratch,
-                           static_cast<size_t>(MXQ_NOALLOC_SCRATCH_BYTES), stream);
+                           need > 0 ? static_cast<size_t>(MXQ_NOALLOC_SCRATCH_BYTES) : 0, stream);
 }

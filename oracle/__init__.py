@@ -88,6 +88,8 @@ def _load():
         lib.oracle_fused_experts.restype = I32
         lib.oracle_fused_experts.argtypes = [P, I64, I64, I64, I32, I32, I64, P, P, P,
                                              P, P, P, P, P, I32, P, I64, P, P]
+        lib.oracle_expert_linear.restype = None
+        lib.oracle_expert_linear.argtypes = [P, I64, I64, I32, P, P, I64, I64, I64, P]
         lib.oracle_max_threads.restype = I32
         lib.oracle_set_threads.argtypes = [I32]
         _lib = lib
@@ -282,6 +284,24 @@ def fused_experts(hidden_bits, wtype, w1, w1_scale, b1, w2, w2_scale, b2,
         raise ValueError("oracle_fused_experts failed with code %d" % rc)
     if checkpoints:
         return out, act, z
+    return out
+
+
+def expert_linear(x_bits, wtype, w, w_scale, e: int):
+    """One expert GEMM without bias, fp64: x [M, C] (bf16 bits) . W[e]^T.
+
+    w: [E, R, C] e4m3 (w_scale fp32 [E, ceil(R/128), ceil(C/128)]) or
+    [E, R, C/2] packed e2m1 (w_scale ue8m0 [E, R, C/32]).  Returns [M, R]."""
+    lib = _load()
+    x = _c(x_bits, np.uint16)
+    M, C = x.shape
+    w = _c(w, np.uint8)
+    R = w.shape[1]
+    w_scale = _c(w_scale, np.uint8 if wtype == W_MXFP4 else np.float32)
+    if not 0 <= e < w.shape[0]:
+        raise ValueError("expert index out of range")
+    out = np.empty((M, R), dtype=np.float64)
+    lib.oracle_expert_linear(_ptr(x), M, C, wtype, _ptr(w), _ptr(w_scale), e, R, C, _ptr(out))
     return out
 
 

@@ -376,6 +376,23 @@ static double expert_row_dot(int32_t wtype, const void* w, const void* ws, int64
   return acc;
 }
 
+/* One expert GEMM of the fused MoE without its bias, the stage accumulators
+ * of [vLLM-50949] (stage 1: hidden . W1[e]^T; stage 2: act . W2[e]^T):
+ *   out[m, r] = sum_k x[m, k] * W[e][r][k]   (format scales as above, fp64)
+ * x bf16 [M, C] row stride ldx; W [E, R, C] in either format; out fp64
+ * [M, R].  Used to check a GPU stage accumulator on the GPU's own inputs. */
+void oracle_expert_linear(const uint16_t* x, int64_t M, int64_t ldx, int32_t wtype,
+                          const void* w, const void* ws, int64_t e, int64_t R, int64_t C,
+                          double* out) {
+  double* a = (double*)malloc(sizeof(double) * (M * C > 0 ? M * C : 1));
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t k = 0; k < C; ++k) a[m * C + k] = oracle_bf16_decode(x[m * ldx + k]);
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int64_t i = 0; i < M * R; ++i)
+    out[i] = expert_row_dot(wtype, w, ws, e, R, C, i % R, a + (i / R) * C);
+  free(a);
+}
+
 /* Routed fused MoE of [vLLM-50949] (stage 1 hidden @ w1, activation,
  * stage 2 @ w2) followed by the top-k weighted combine:
  *   for each slot (t, k), e = topk_ids[t,k]:

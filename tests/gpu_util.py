@@ -57,3 +57,34 @@ def assert_sampled_close(got, ref, rowmax, rel=1e-3, floor=1e-2, what="sampled a
         i = np.nonzero(bad)[0][:5]
         raise AssertionError("%s: %d of %d outside tolerance, e.g. got %s ref %s" % (
             what, bad.sum(), bad.size, g[i], r[i]))
+
+
+def moe_stage_probes(oracle, wtype, x_bits, ids, tw, expert, act, y, h, slots):
+    """The two fp32 stage accumulators of the fused MoE at the given slots
+    (slot = t*topk + k), each against the oracle's per-expert GEMM fed with
+    the GPU's own stage input, at the fp32 accumulator tolerance:
+        h[slot] = x[t] . W1[e]^T                 (before the bias)
+        y[slot] = w[slot] * (act[slot] . W2[e]^T + b2[e])
+    x_bits: bf16 bits [T, K]; ids / tw: [T, topk] (CPU); act, y, h: GPU
+    checkpoints in slot order; expert(e) -> (w1, s1, w2, s2, b2) of expert e
+    alone as numpy arrays with a leading dimension of one (b2 may be None)."""
+    ids_f = np.asarray(ids).reshape(-1)
+    tw_f = np.asarray(tw, np.float64).reshape(-1)
+    topk = np.asarray(ids).shape[1]
+    slots = np.asarray(sorted(slots), np.int64)
+    sl_t = torch.from_numpy(slots).to(act.device)
+    act_b = bits16(act[sl_t])
+    h_g = h[sl_t].double().cpu().numpy()
+    y_g = y[sl_t].double().cpu().numpy()
+    h_r = np.empty_like(h_g)
+    y_r = np.empty_like(y_g)
+    for e in np.unique(ids_f[slots]):
+        sel = np.nonzero(ids_f[slots] == e)[0]
+        w1, s1, w2, s2, b2 = expert(int(e))
+        h_r[sel] = oracle.expert_linear(x_bits[slots[sel] // topk], wtype, w1, s1, 0)
+        z = oracle.expert_linear(act_b[sel], wtype, w2, s2, 0)
+        if b2 is not None:
+            z = z + np.asarray(b2, np.float64).reshape(1, -1)
+        y_r[sel] = tw_f[slots[sel]].reshape(-1, 1) * z
+    assert_probe_close(h_g, h_r, what="stage-1 accumulator h")
+    assert_probe_close(y_g, y_r, what="stage-2 accumulator y")

@@ -96,6 +96,28 @@ def test_scaled_mm_argument_errors(lib):
     assert mm(lib, W=ctypes.c_void_p((1 << 20) + 8)) == _lib.ERR_UNSUPPORTED
 
 
+def test_workspace_query_and_noalloc_validate_before_any_device_work(lib):
+    """The split-K workspace query takes the block size the call will get and
+    refuses the same illegal ones; the allocation-free GEMM reports a bad
+    argument as itself (not as a scratch-size problem), whatever the shape."""
+    from mxfp4_quantized_gemm_token_gb300 import _lib
+    sz = ctypes.c_size_t(7)
+    q = lib.mxq_fp8_scaled_mm_workspace_size
+    assert q(4, 128, 256, 3, 1, 32, ctypes.byref(sz)) == _lib.ERR_UNSUPPORTED     # MXFP8 [1, 32]
+    assert q(4, 128, 256, 7, 128, 128, ctypes.byref(sz)) == _lib.ERR_UNSUPPORTED   # a_dtype
+    assert q(4, 128, 0, 3, 128, 128, ctypes.byref(sz)) == _lib.ERR_INVALID_ARG
+    assert q(4, 128, 256, 3, 128, 128, None) == _lib.ERR_INVALID_ARG
+    na = lib.mxq_fp8_scaled_mm_noalloc
+    base = [FAKE, 3, 4096, 4096, 4096, FAKE, 32, 1, FAKE, 4096, 4096, FAKE, 128, 128, 32, 1,
+            None, 0, FAKE, 1, 4096]
+    for i, v, st in [(0, None, _lib.ERR_INVALID_ARG), (5, None, _lib.ERR_INVALID_ARG),
+                     (12, 2, _lib.ERR_UNSUPPORTED), (19, 3, _lib.ERR_UNSUPPORTED)]:
+        args = list(base)
+        args[i] = v
+        assert na(*args, None) == st
+        assert b"scratch" not in lib.mxq_last_error()
+
+
 def test_quant_align_moe_argument_errors(lib):
     from mxfp4_quantized_gemm_token_gb300 import _lib
     q = lib.mxq_per_token_group_quant_fp8

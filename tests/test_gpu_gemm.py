@@ -190,6 +190,16 @@ def big_w128():
     return wq, ws, u8(wq), ws.cpu().numpy()
 
 
+def sample_rows(M):
+    """Row 0, the last row, and one row of every 128-token tile (at a
+    varying offset inside the tile), so every token tile of the launch is
+    checked."""
+    rows = {0, M - 1, M // 2, (M * 7) // 11}
+    for t in range((M + 127) // 128):
+        rows.add(min(M - 1, t * 128 + (t * 37 + 5) % 128))
+    return sorted(rows)
+
+
 @pytest.mark.parametrize("M", [1, 8, 17, 128, 1024, 4096])
 def test_full_size_block128_sampled_rows(oracle, big_w128, M):
     wq, ws, w_np, ws_np = big_w128
@@ -197,7 +207,7 @@ def test_full_size_block128_sampled_rows(oracle, big_w128, M):
     q, s = mxq.per_token_group_quant_fp8(x)
     o32 = mxq.fp8_scaled_mm(q, wq, ws, [128, 128], a_scale=s, out_dtype=torch.float32)
     o16 = mxq.fp8_scaled_mm(q, wq, ws, [128, 128], a_scale=s)
-    rows = sorted(set([0, M - 1, M // 2, (M * 7) // 11]))
+    rows = sample_rows(M)
     ridx = torch.tensor(rows, device="cuda")
     rq, rs = oracle.per_token_group_quant_fp8(bits16(x[ridx]), 128)
     rf, rb = oracle.scaled_mm(rq, E4M3, rs, w_np, ws_np, 128, 128)
@@ -217,11 +227,15 @@ def test_full_size_block1x128_sampled_rows(oracle, M):
     assert out.shape == (*x.shape[:-1], 4096)
     flat = out.reshape(-1, 4096)
     xf = x.reshape(-1, 7168)
-    rows = sorted(set([0, M - 1, M // 3]))
+    # the fp32 accumulator of the same call (quantized input, same plan)
+    q, s = mxq.per_token_group_quant_fp8(xf)
+    o32 = mxq.fp8_scaled_mm(q, wq, ws, [1, 128], a_scale=s, out_dtype=torch.float32)
+    rows = sample_rows(M)
     ridx = torch.tensor(rows, device="cuda")
     rq, rs = oracle.per_token_group_quant_fp8(bits16(xf[ridx]), 128)
-    _, rb = oracle.scaled_mm(rq, E4M3, rs, u8(wq), ws.cpu().numpy(), 1, 128)
+    rf, rb = oracle.scaled_mm(rq, E4M3, rs, u8(wq), ws.cpu().numpy(), 1, 128)
     assert_bf16_close(flat[ridx], rb)
+    assert_probe_close(o32[ridx], rf)
 
 
 @pytest.mark.parametrize("tile", [128, 192, 256])
@@ -261,3 +275,57 @@ def test_forced_token_tile_widths(oracle, tile):
         assert_bf16_close(o, rb)
     finally:
         mxq.set_option(_lib.OPT_TILE_N, 0)
+
+
+@pytest.mark.parametrize("case", ["block128_decode", "block1x128_large_m", "block1x128_decode",
+                                  "per_tensor_bf16"])
+def test_workspace_query_describes_the_call(case):
+    """The split-K workspace query takes the call's activation type and block
+    size, so it sizes the plan the call runs: with exactly that many bytes the
+    call succeeds, with 16 fewer (when the plan splits) it is refused, and the
+    result equals the no-split run within the accumulator tolerance."""
+    import ctypes
+    lib = _lib.load()
+    M, N, K, bn, a_dt = {"block128_decode": (8, 4096, 7168, 128, E4M3),
+                         "block1x128_large_m": (512, 4608, 7168, 1, E4M3),
+                         "block1x128_decode": (4, 4096, 7168, 1, E4M3),
+                         "per_tensor_bf16": (8, 4096, 7168, 0, BF16)}[case]
+    bk = 0 if bn == 0 else 128
+    x = synth.activations(M, K, seed=90, device="cuda")
+    if bn == 0:
+        _, w, _, _ = synth.per_tensor_fp8_problem(M=M, N=N, K=K, seed=91)
+        w, ws = w.cuda(), torch.full((1,), 0.01, device="cuda")
+        a, s = x, None
+    else:
+        w, ws = synth.block_fp8_weight(N, K, bn, seed=91, device="cuda")
+        a, s = mxq.per_token_group_quant_fp8(x)
+    sz = ctypes.c_size_t(0)
+    assert lib.mxq_fp8_scaled_mm_workspace_size(M, N, K, a_dt, bn, bk, ctypes.byref(sz)) == 0
+    need = sz.value
+    ref = mxq.fp8_scaled_mm(a, w, ws, None if bn == 0 else [bn, bk], a_scale=s,
+                            out_dtype=torch.float32, workspace=torch.empty(0, dtype=torch.uint8,
+                                                                           device="cuda"))
+    nosplit = torch.empty_like(ref)
+
+    def call(out, work, nbytes):
+        return lib.mxq_fp8_scaled_mm(
+            ctypes.c_void_p(a.data_ptr()), a_dt, M, K, K,
+            None if s is None else ctypes.c_void_p(s.data_ptr()), 0 if s is None else s.stride(0),
+            0 if s is None else s.stride(1), ctypes.c_void_p(w.data_ptr()), N, K,
+            ctypes.c_void_p(ws.data_ptr()), bn, bk, ws.stride(0) if ws.dim() == 2 else 0,
+            ws.stride(1) if ws.dim() == 2 else 0, None, 0, ctypes.c_void_p(out.data_ptr()),
+            _lib.F32, N, None if work is None else ctypes.c_void_p(work.data_ptr()), nbytes,
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+    assert call(nosplit, None, 0) == 0
+    if need > 0:
+        work = torch.empty(need, dtype=torch.uint8, device="cuda")
+        assert call(ref, work, need - 16) == _lib.ERR_INVALID_ARG
+        assert b"workspace" in lib.mxq_last_error()
+        assert call(ref, work, need) == 0
+    else:
+        assert call(ref, None, 0) == 0
+    torch.cuda.synchronize()
+    assert_probe_close(ref, nosplit.double().cpu().numpy())
+    # the expected plans: decode-size shapes split, the [1, 128] large-M one does not
+    assert (need > 0) == (M <= 8)

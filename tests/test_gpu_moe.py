@@ -10,7 +10,7 @@ import torch
 
 import mxfp4_quantized_gemm_token_gb300 as mxq
 from mxfp4_quantized_gemm_token_gb300 import _lib, synth
-from gpu_util import assert_bf16_close, bits16, u8
+from gpu_util import assert_bf16_close, bits16, moe_stage_probes, u8
 
 pytestmark = pytest.mark.gpu
 W_FP8, W_MX = 1, 2
@@ -63,23 +63,30 @@ def weights(wtype, E, N, K, seed, bias):
     return w1, s1, w2, s2, b1, b2
 
 
-def run_moe(oracle, wtype, E, N, K, x, tw, ids, block_m, seed=1, bias=False, check_ckpt=True):
-    w1, s1, w2, s2, b1, b2 = weights(wtype, E, N, K, seed, bias)
+def run_moe(oracle, wtype, E, N, K, x, tw, ids, block_m, seed=1, bias=False, check_ckpt=True,
+            wts=None):
+    w1, s1, w2, s2, b1, b2 = weights(wtype, E, N, K, seed, bias) if wts is None else wts
     sc = (lambda s: u8(s)) if wtype == W_MX else (lambda s: s.numpy())
     ref, ract, rz = oracle.fused_experts(
         bits16(x), wtype, u8(w1), sc(s1), None if b1 is None else b1.numpy(), u8(w2), sc(s2),
         None if b2 is None else b2.numpy(), tw.numpy(), ids.numpy(), N, checkpoints=True)
     cu = lambda t: None if t is None else t.cuda()
-    out, act, y = mxq.fused_experts(cu(x), cu(w1), cu(s1), cu(w2), cu(s2), cu(tw), cu(ids),
-                                    wtype=wtype, w1_bias=cu(b1), w2_bias=cu(b2),
-                                    block_m=block_m, checkpoints=True)
+    out, act, y, h = mxq.fused_experts(cu(x), cu(w1), cu(s1), cu(w2), cu(s2), cu(tw), cu(ids),
+                                       wtype=wtype, w1_bias=cu(b1), w2_bias=cu(b2),
+                                       block_m=block_m, checkpoints=True)
+    plain = mxq.fused_experts(cu(x), cu(w1), cu(s1), cu(w2), cu(s2), cu(tw), cu(ids),
+                              wtype=wtype, w1_bias=cu(b1), w2_bias=cu(b2), block_m=block_m)
     mxq.sync_status()
+    assert torch.equal(plain, out)          # the checkpoints do not change the result
     assert_bf16_close(out, ref, what="moe output")
     if check_ckpt:
         assert_bf16_close(act, ract, what="act checkpoint")
-        yref = rz * tw.numpy().reshape(-1, 1).astype(np.float64)
-        scale = np.abs(yref).max(axis=1, keepdims=True)
-        assert np.all(np.abs(y.double().cpu().numpy() - yref) <= 2e-2 * (np.abs(yref) + 0.05 * scale))
+
+        def expert(e):
+            return (u8(w1[e:e + 1]), sc(s1[e:e + 1]), u8(w2[e:e + 1]), sc(s2[e:e + 1]),
+                    None if b2 is None else b2[e].numpy())
+        moe_stage_probes(oracle, wtype, bits16(x), ids.numpy(), tw.numpy(), expert, act, y, h,
+                         range(ids.numel()))
     return out
 
 
@@ -138,15 +145,20 @@ def test_fused_small_expert_blocks_4_5_33(oracle, topk):
     T = ids.shape[0]
     N, K = 128, 256
     x = synth.activations(T, K, seed=9, scale_div=10)
-    run_moe(oracle, W_FP8, E, N, K, x, tw, ids, 16, check_ckpt=(topk == 1))
+    run_moe(oracle, W_FP8, E, N, K, x, tw, ids, 16)
 
 
-def test_fused_narrow_and_wide_paths_agree(oracle):
+@pytest.mark.parametrize("N,K", [(128, 256), (160, 224)])
+def test_fused_narrow_and_wide_paths_agree(oracle, N, K):
     """Per-block choice (threshold 4), always narrow, always full width and one
-    path for the whole layer all give the oracle's result."""
-    E, N, K, T, topk = 8, 128, 256, 21, 2
+    path for the whole layer all give the oracle's result, also when the
+    last weight tile of each stage is a ragged tail (N = 160: the SiLU
+    stage's last 64-row tile holds 32 rows; K = 224: stage 2's last 128-row
+    tile holds 96)."""
+    E, T, topk = 8, 21, 2
     x = synth.activations(T, K, seed=11, scale_div=10)
     tw, ids = synth.routing_zipf(T, E, topk, seed=12)
+    old = mxq.get_option(_lib.OPT_SMALL_M_MAX)
     try:
         mxq.set_option(_lib.OPT_SMALL_M_MAX, 4)
         for force in (0, 1, 2, 3):
@@ -155,4 +167,20 @@ def test_fused_narrow_and_wide_paths_agree(oracle):
             run_moe(oracle, W_MX, E, N, K, x, tw, ids, 64)
     finally:
         mxq.set_option(_lib.OPT_FORCE_PATH, 0)
-        mxq.set_option(_lib.OPT_SMALL_M_MAX, 1 << 30)
+        mxq.set_option(_lib.OPT_SMALL_M_MAX, old)
+
+
+def test_fused_mxfp4_scales_beyond_bf16_single_step(oracle):
+    """ue8m0 exponents of 143 and above (scales of 2^16 and more, which the
+    decode folds into the bf16 weights in two multiplications) in stage 1,
+    and small ones in stage 2, against the oracle, with the stage
+    accumulators checked too."""
+    E, N, K, T, topk = 4, 128, 256, 9, 2
+    w1, s1, w2, s2 = synth.moe_mxfp4_weights(E, N, K, seed=51)
+    s1 = (s1.to(torch.int32) + 21).clamp(max=254).to(torch.uint8)   # 141 .. 143
+    s2 = (s2.to(torch.int32) - 21).clamp(min=1).to(torch.uint8)
+    assert bool((s1 >= 143).any()) and bool((s1 < 143).any())
+    b1, b2 = synth.moe_biases(E, N, K, seed=52)
+    x = synth.activations(T, K, seed=53, scale_div=10)
+    tw, ids = synth.routing_uniform(T, E, topk, seed=54)
+    run_moe(oracle, W_MX, E, N, K, x, tw, ids, 16, wts=(w1, s1, w2, s2, b1, b2))

@@ -265,3 +265,25 @@ def test_topk_combine_matches_weighted_dense_mlps(oracle, wtype, topk, E):
             o += float(tw[t, k]) * rz
         ref = o.float().to(torch.bfloat16).float()
         assert torch.equal(bf16_of(out[t]).float(), ref), t
+
+
+@pytest.mark.parametrize("wtype", [W_FP8, W_MX])
+def test_expert_linear_matches_dequantised_matmul(oracle, wtype):
+    """The per-expert GEMM (the stage accumulators h and z without bias)
+    against a library fp64 matmul of independently dequantised weights, for
+    every expert, with ragged 128-blocks in both dimensions (FP8)."""
+    E, R, C, M = 3, 320 if wtype == W_FP8 else 192, 384 if wtype == W_FP8 else 288, 4
+    if wtype == W_FP8:
+        w1, s1, _, _ = synth.moe_fp8_weights(E, R // 2, C, seed=41)
+        W = deq_fp8(w1, s1)
+        sc = s1.numpy()
+    else:
+        w1, s1, _, _ = synth.moe_mxfp4_weights(E, R // 2, C, seed=41)
+        W = deq_mx(w1, s1)
+        sc = u8(s1)
+    x = synth.activations(M, C, seed=42, scale_div=10)
+    for e in range(E):
+        got = oracle.expert_linear(bits(x), wtype, u8(w1), sc, e)
+        ref = (x.double() @ W[e].T).numpy()
+        assert got.shape == (M, R)
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-15), e
