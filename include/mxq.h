@@ -179,6 +179,45 @@ mxq_status mxq_fp8_scaled_mm_noalloc(const void* A, int32_t a_dtype, int64_t M, 
                                      const void* bias, int32_t bias_dtype, void* out,
                                      int32_t out_dtype, int64_t ldo, mxq_stream_t stream);
 
+/*
+ * Load-time weight prepack for mxq_fp8_scaled_mm ([CPU-GEMM], implementation
+ * breakdown: the FP8 weight is transposed and packed once after loading into
+ * the layout the kernel reads; [XPU-FP8], process_weights_after_loading_block_quant:
+ * the block scales are stored transposed-contiguous).  Here:
+ *   Wp    ceil(N/128) * ceil(K/128) tiles of 16384 bytes; tile (tn, kb) at
+ *         byte offset (tn * ceil(K/128) + kb) * 16384 holds rows
+ *         tn*128 .. tn*128+127 and K bytes kb*128 .. kb*128+127 of W as the
+ *         tensor core's 128-byte-swizzled operand image: byte b of 16-byte
+ *         chunk c of tile row r at r*128 + ((c ^ (r % 8)) * 16) + b.  Rows
+ *         past N and columns past K are zero.  256-byte aligned.
+ *   ws_p  block scales K-block-major: Ws[nb, kb] at ws_p[kb * ceil(N/bn) + nb]
+ *         ([ceil(K/128), ceil(N/bn)] contiguous); per-tensor: the one scale.
+ *   W, w_scale, block_n, block_k, sw0, sw1 as in mxq_fp8_scaled_mm (W row
+ *   stride ldw, a multiple of 16).  Sizes of Wp and ws_p come from
+ *   mxq_prepacked_weight_size.  Asynchronous on `stream`.
+ */
+mxq_status mxq_prepacked_weight_size(int64_t N, int64_t K, int32_t block_n, int32_t block_k,
+                                     size_t* w_bytes, size_t* s_bytes);
+mxq_status mxq_prepack_weight(const void* W, int64_t N, int64_t K, int64_t ldw,
+                              const float* w_scale, int32_t block_n, int32_t block_k, int64_t sw0,
+                              int64_t sw1, void* Wp, float* ws_p, mxq_stream_t stream);
+
+/*
+ * mxq_fp8_scaled_mm with weights prepacked by mxq_prepack_weight (Wp, ws_p
+ * for the same N, K, block_n, block_k).  Every other argument, the split-K
+ * plan and its workspace (mxq_fp8_scaled_mm_workspace_size) are those of
+ * mxq_fp8_scaled_mm, and the result is bit-identical to it: only the way
+ * the weight tiles reach shared memory differs (one contiguous bulk copy per
+ * tile instead of a tensor-map copy of 128 strided rows).
+ */
+mxq_status mxq_fp8_scaled_mm_prepacked(const void* A, int32_t a_dtype, int64_t M, int64_t K,
+                                       int64_t lda, const float* a_scale, int64_t sa0, int64_t sa1,
+                                       const void* Wp, int64_t N, const float* ws_p,
+                                       int32_t block_n, int32_t block_k, const void* bias,
+                                       int32_t bias_dtype, void* out, int32_t out_dtype,
+                                       int64_t ldo, void* workspace, size_t ws_bytes,
+                                       mxq_stream_t stream);
+
 /* Workspace bytes of the split-K plan mxq_fp8_scaled_mm runs for this shape
  * on the current device (0 when it does not split).  The plan depends on the
  * activation type and the weight block size (a_dtype, block_n, block_k take

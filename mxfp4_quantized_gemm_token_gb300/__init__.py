@@ -23,6 +23,7 @@ from ._lib import MxqError, check
 
 __all__ = [
     "MxqError", "per_token_group_quant_fp8", "fp8_scaled_mm", "w8a8_block_fp8_linear",
+    "PackedWeight", "prepack_weight",
     "fp8_per_tensor_linear", "moe_align_block", "fused_experts", "align_capacity",
     "set_option", "get_option", "sync_status", "W_FP8_BLOCK128", "W_MXFP4",
 ]
@@ -96,6 +97,47 @@ def _as_rows(t: torch.Tensor):
     return t2
 
 
+class PackedWeight:
+    """An e4m3 weight [N, K] and its scales after mxq_prepack_weight: the
+    tiles (uint8, 16384 bytes per 128 x 128 tile) and the K-block-major
+    scales.  Pass it as ``w`` to fp8_scaled_mm / w8a8_block_fp8_linear."""
+
+    def __init__(self, tiles, scales, N, K, block_size):
+        self.tiles, self.scales, self.N, self.K = tiles, scales, N, K
+        self.block_size = None if block_size is None else [int(b) for b in block_size]
+        self.device = tiles.device
+
+    @property
+    def shape(self):
+        return (self.N, self.K)
+
+
+def prepack_weight(w, w_scale, block_size=None) -> PackedWeight:
+    """Load-time relayout of an e4m3 weight [N, K] (any row stride with unit
+    inner stride) and its scales (per-tensor, or [ceil(N/bn), ceil(K/128)]
+    with any strides) into the tile layout the GEMM streams."""
+    _need_cuda(w, w_scale)
+    lib = _lib_handle()
+    if w.stride(-1) != 1:
+        w = w.contiguous()
+    N, K = w.shape
+    bn, bk = (0, 0) if block_size is None else (int(block_size[0]), int(block_size[1]))
+    sw0 = sw1 = 0
+    if block_size is not None:
+        if w_scale.dim() != 2:
+            raise ValueError("block weight scales must be 2-D")
+        sw0, sw1 = w_scale.stride(0), w_scale.stride(1)
+    elif w_scale.numel() != 1:
+        raise ValueError("per-tensor scale must have one element")
+    wb, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    check(lib.mxq_prepacked_weight_size(N, K, bn, bk, ctypes.byref(wb), ctypes.byref(sb)))
+    tiles = torch.empty(max(wb.value, 1), dtype=torch.uint8, device=w.device)
+    scales = torch.empty(max(sb.value // 4, 1), dtype=torch.float32, device=w.device)
+    check(lib.mxq_prepack_weight(_ptr(w), N, K, w.stride(0), _ptr(w_scale), bn, bk, sw0, sw1,
+                                 _ptr(tiles), _ptr(scales), _stream(w.device)))
+    return PackedWeight(tiles, scales, N, K, block_size)
+
+
 def fp8_scaled_mm(a, w, w_scale, block_size=None, a_scale=None, bias=None,
                   out_dtype=torch.bfloat16, workspace=None):
     """out[..., N] = sum_k a[..., k] w[n, k] * scales (+ bias).
@@ -104,18 +146,33 @@ def fp8_scaled_mm(a, w, w_scale, block_size=None, a_scale=None, bias=None,
     [..., K] with a_scale None (W8A16); w: e4m3 [N, K]; w_scale: fp32 0-d/[1]
     (per-tensor, block_size None) or [ceil(N/bn), ceil(K/128)] with
     block_size [bn, 128], bn in {1, 128}, any strides.
+    w may also be a PackedWeight (prepack_weight), with w_scale None and the
+    block_size it was packed with; the result is bit-identical.
     workspace: None (the library's split-K plan, sized by the workspace
     query and allocated here) or a caller buffer of at least that size; an
     empty buffer runs without split-K.
     """
-    _need_cuda(a, w, w_scale, a_scale, bias)
+    packed = isinstance(w, PackedWeight)
+    if packed:
+        if w_scale is not None:
+            raise ValueError("a PackedWeight carries its scales: pass w_scale=None")
+        if (block_size is None) != (w.block_size is None) or (
+                block_size is not None and list(block_size) != w.block_size):
+            raise ValueError("block_size %r does not match the packed weight's %r"
+                             % (block_size, w.block_size))
+        if a.shape[-1] != w.K:
+            raise ValueError("K of the input (%d) and of the packed weight (%d) differ"
+                             % (a.shape[-1], w.K))
+        _need_cuda(a, w.tiles, a_scale, bias)
+    else:
+        _need_cuda(a, w, w_scale, a_scale, bias)
     lib = _lib_handle()
     K = a.shape[-1]
     a2 = _as_rows(a)
     M = a2.shape[0]
-    if w.stride(-1) != 1:
+    if not packed and w.stride(-1) != 1:
         w = w.contiguous()
-    N = w.shape[0]
+    N = w.N if packed else w.shape[0]
     if a.dtype == torch.float8_e4m3fn:
         a_dtype = _lib.E4M3
     elif a.dtype == torch.bfloat16:
@@ -129,15 +186,16 @@ def fp8_scaled_mm(a, w, w_scale, block_size=None, a_scale=None, bias=None,
     if block_size is None:
         bn = bk = 0
         sw0 = sw1 = 0
-        if w_scale.numel() != 1:
+        if not packed and w_scale.numel() != 1:
             raise ValueError("per-tensor scale must have one element")
     else:
         if not isinstance(block_size, (list, tuple)) or len(block_size) != 2:
             raise ValueError("block_size must be a two-element list, got %r" % (block_size,))
         bn, bk = int(block_size[0]), int(block_size[1])
-        if w_scale.dim() != 2:
-            raise ValueError("block weight scales must be 2-D")
-        sw0, sw1 = w_scale.stride(0), w_scale.stride(1)
+        if not packed:
+            if w_scale.dim() != 2:
+                raise ValueError("block weight scales must be 2-D")
+            sw0, sw1 = w_scale.stride(0), w_scale.stride(1)
     bias_dtype = 0
     if bias is not None:
         if bias.dtype not in (torch.bfloat16, torch.float32):
@@ -154,17 +212,24 @@ def fp8_scaled_mm(a, w, w_scale, block_size=None, a_scale=None, bias=None,
             workspace = torch.empty(sz.value, dtype=torch.uint8, device=a.device)
     if workspace is not None:
         ws_bytes = workspace.numel() * workspace.element_size()
-    check(lib.mxq_fp8_scaled_mm(
-        _ptr(a2), a_dtype, M, K, a2.stride(0), _ptr(a_scale), sa0, sa1, _ptr(w), N, w.stride(0),
-        _ptr(w_scale), bn, bk, sw0, sw1, _ptr(bias), bias_dtype, _ptr(out), od, N,
-        _ptr(workspace) if ws_bytes else None, ws_bytes, _stream(a.device)))
+    if packed:
+        check(lib.mxq_fp8_scaled_mm_prepacked(
+            _ptr(a2), a_dtype, M, K, a2.stride(0), _ptr(a_scale), sa0, sa1, _ptr(w.tiles), N,
+            _ptr(w.scales), bn, bk, _ptr(bias), bias_dtype, _ptr(out), od, N,
+            _ptr(workspace) if ws_bytes else None, ws_bytes, _stream(a.device)))
+    else:
+        check(lib.mxq_fp8_scaled_mm(
+            _ptr(a2), a_dtype, M, K, a2.stride(0), _ptr(a_scale), sa0, sa1, _ptr(w), N,
+            w.stride(0), _ptr(w_scale), bn, bk, sw0, sw1, _ptr(bias), bias_dtype, _ptr(out), od,
+            N, _ptr(workspace) if ws_bytes else None, ws_bytes, _stream(a.device)))
     return out.view(*a.shape[:-1], N)
 
 
 def w8a8_block_fp8_linear(input, weight, block_size, weight_scale, input_scale=None, bias=None):
     """Block-FP8 linear with the pages' semantics: quantize the input per
     1x128 group unless input_scale is given; output bf16 for a pre-quantized
-    input, else input.dtype; batch dims restored."""
+    input, else input.dtype; batch dims restored.  weight may be a
+    PackedWeight (prepack_weight), with weight_scale None."""
     if not isinstance(block_size, (list, tuple)) or len(block_size) != 2:
         raise ValueError("block_size must be a two-element list, got %r" % (block_size,))
     bn, bk = block_size

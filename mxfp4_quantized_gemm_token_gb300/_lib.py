@@ -27,6 +27,7 @@ EXPORTED = [
     "mxq_per_token_group_quant_fp8", "mxq_fp8_scaled_mm", "mxq_fp8_scaled_mm_workspace_size",
     "mxq_moe_align_block", "mxq_fused_experts", "mxq_fused_experts_debug",
     "mxq_fused_experts_workspace_size", "mxq_fp8_scaled_mm_noalloc",
+    "mxq_prepacked_weight_size", "mxq_prepack_weight", "mxq_fp8_scaled_mm_prepacked",
 ]
 
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -55,6 +56,11 @@ def _declare(lib):
                                            I32, I32, I64, I64, P, I32, P, I32, I64, P]),
         "mxq_fp8_scaled_mm_workspace_size": (st, [I64, I64, I64, I32, I32, I32,
                                                   ctypes.POINTER(SZ)]),
+        "mxq_prepacked_weight_size": (st, [I64, I64, I32, I32, ctypes.POINTER(SZ),
+                                           ctypes.POINTER(SZ)]),
+        "mxq_prepack_weight": (st, [P, I64, I64, I64, P, I32, I32, I64, I64, P, P, P]),
+        "mxq_fp8_scaled_mm_prepacked": (st, [P, I32, I64, I64, I64, P, I64, I64, P, I64, P, I32,
+                                             I32, P, I32, P, I32, I64, P, SZ, P]),
         "mxq_moe_align_block": (st, [P, I64, I32, I32, I32, P, P, P, P, I64, P, SZ, P]),
         "mxq_fused_experts": (st, [P, I64, I64, I64, I32, I32, I64, P, P, P, P, P, P, P, P, I32,
                                    I32, P, I64, P, SZ, P]),

@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmxq.so")
 
-SOURCES = ["api.cu", "quant.cu", "moe_aux.cu", "gemm_dense.cu", "gemm_moe.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "quant.cu", "moe_aux.cu", "gemm_dense.cu", "gemm_moe.cu", "noalloc.cu",
+           "prepack.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

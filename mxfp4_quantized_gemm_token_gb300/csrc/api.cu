@@ -227,11 +227,10 @@ MmPlan plan_mm(int64_t M, int64_t N, int64_t K, int32_t a_dtype, bool block, boo
   pl.normal = pl.kind == KIND_F8F8 && has_ascale && uniform_wscale && M > 128 && tile == 0;
   if (pl.normal) {
     const int64_t nt = option(MXQ_OPT_NORMAL_TILE);
-    // 192-wide weight tiles keep the epilogue's 64 accumulators per thread
-    // clear of spills (512 threads); 256 packs fewer waves when the token
-    // count is small
-    pl.bt = nt > 0 ? static_cast<int>(nt)
-                   : (N < 4096 ? 128 : (M >= 1024 ? 192 : (M >= 512 ? 256 : 128)));
+    // 128-wide weight tiles: four TMEM accumulator buffers (one per slice in
+    // flight) and two epilogue warpgroups of 64 columns; measured faster than
+    // 192 (two buffers) and 256 (the epilogue spills) at M = 1024 and 4096
+    pl.bt = nt > 0 ? static_cast<int>(nt) : 128;
   }
   pl.promote = block || has_ascale;
   pl.tiles_n = static_cast<int>(cdiv(N, pl.normal ? pl.bt : 128));
@@ -350,19 +349,17 @@ extern "C" mxq_status mxq_fp8_scaled_mm_workspace_size(int64_t M, int64_t N, int
   return mm_workspace_bytes(M, N, K, a_dtype, block_n, block_k, bytes);
 }
 
-extern "C" mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t M, int64_t K,
-                                        int64_t lda, const float* a_scale, int64_t sa0,
-                                        int64_t sa1, const void* W, int64_t N, int64_t ldw,
-                                        const float* w_scale, int32_t block_n, int32_t block_k,
-                                        int64_t sw0, int64_t sw1, const void* bias,
-                                        int32_t bias_dtype, void* out, int32_t out_dtype,
-                                        int64_t ldo, void* workspace, size_t ws_bytes,
-                                        mxq_stream_t stream) {
-  const mxq_status vst = validate_mm(A, a_dtype, M, K, lda, a_scale, sa0, sa1, W, N, ldw, w_scale,
-                                     block_n, block_k, sw0, sw1, bias, bias_dtype, out, out_dtype,
-                                     ldo);
-  if (vst != MXQ_OK) return vst;
-  if (M == 0 || N == 0) return MXQ_OK;
+namespace {
+
+// The scaled GEMM for validated arguments with M, N > 0.  W is the weight
+// matrix (row stride ldw) or, when wpacked is set, unused: the weights are
+// then the prepacked tiles of mxq_prepack_weight.
+mxq_status scaled_mm_run(const void* A, int32_t a_dtype, int64_t M, int64_t K, int64_t lda,
+                         const float* a_scale, int64_t sa0, int64_t sa1, const void* W, int64_t N,
+                         int64_t ldw, const uint8_t* wpacked, const float* w_scale,
+                         int32_t block_n, int32_t block_k, int64_t sw0, int64_t sw1,
+                         const void* bias, int32_t bias_dtype, void* out, int32_t out_dtype,
+                         int64_t ldo, void* workspace, size_t ws_bytes, mxq_stream_t stream) {
   const bool per_tensor = block_n == 0 && block_k == 0;
   if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 15) != 0)
     return fail(MXQ_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
@@ -392,10 +389,12 @@ extern "C" mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t 
     // MMA A = tokens (128-row boxes), MMA B = weights (bt-row boxes)
     if (!make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, lda, 128, 128,
                      CU_TENSOR_MAP_SWIZZLE_128B, &err) ||
-        !make_map_2d(&maps.b[bv], CU_TENSOR_MAP_DATA_TYPE_UINT8, W, K, N, ldw, 128, pl.bt,
-                     CU_TENSOR_MAP_SWIZZLE_128B, &err))
+        (wpacked == nullptr &&
+         !make_map_2d(&maps.b[bv], CU_TENSOR_MAP_DATA_TYPE_UINT8, W, K, N, ldw, 128, pl.bt,
+                      CU_TENSOR_MAP_SWIZZLE_128B, &err)))
       return fail(MXQ_ERR_CUDA, err);
-  } else if (!make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, K, N, ldw, 128, 128,
+  } else if (wpacked == nullptr &&
+             !make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, K, N, ldw, 128, 128,
                           CU_TENSOR_MAP_SWIZZLE_128B, &err)) {
     return fail(MXQ_ERR_CUDA, err);
   }
@@ -433,6 +432,8 @@ extern "C" mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t 
   p.out_dtype = out_dtype;
   p.ldo = ldo;
   p.partial = pl.splits > 1 ? reinterpret_cast<float*>(workspace) : nullptr;
+  p.wpacked = wpacked;
+  p.npad = static_cast<int>(cdiv(N, 128) * 128);
   p.status = d.status;
   p.budget_ns = static_cast<unsigned long long>(option(MXQ_OPT_WAIT_BUDGET_NS));
   p.inject_stall = static_cast<int>(option(MXQ_OPT_INJECT_STALL));
@@ -455,6 +456,46 @@ extern "C" mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t 
     if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
   }
   return MXQ_OK;
+}
+
+}  // namespace
+
+extern "C" mxq_status mxq_fp8_scaled_mm(const void* A, int32_t a_dtype, int64_t M, int64_t K,
+                                        int64_t lda, const float* a_scale, int64_t sa0,
+                                        int64_t sa1, const void* W, int64_t N, int64_t ldw,
+                                        const float* w_scale, int32_t block_n, int32_t block_k,
+                                        int64_t sw0, int64_t sw1, const void* bias,
+                                        int32_t bias_dtype, void* out, int32_t out_dtype,
+                                        int64_t ldo, void* workspace, size_t ws_bytes,
+                                        mxq_stream_t stream) {
+  const mxq_status vst = validate_mm(A, a_dtype, M, K, lda, a_scale, sa0, sa1, W, N, ldw, w_scale,
+                                     block_n, block_k, sw0, sw1, bias, bias_dtype, out, out_dtype,
+                                     ldo);
+  if (vst != MXQ_OK) return vst;
+  if (M == 0 || N == 0) return MXQ_OK;
+  return scaled_mm_run(A, a_dtype, M, K, lda, a_scale, sa0, sa1, W, N, ldw, nullptr, w_scale,
+                       block_n, block_k, sw0, sw1, bias, bias_dtype, out, out_dtype, ldo,
+                       workspace, ws_bytes, stream);
+}
+
+extern "C" mxq_status mxq_fp8_scaled_mm_prepacked(
+    const void* A, int32_t a_dtype, int64_t M, int64_t K, int64_t lda, const float* a_scale,
+    int64_t sa0, int64_t sa1, const void* Wp, int64_t N, const float* ws_p, int32_t block_n,
+    int32_t block_k, const void* bias, int32_t bias_dtype, void* out, int32_t out_dtype,
+    int64_t ldo, void* workspace, size_t ws_bytes, mxq_stream_t stream) {
+  // the packed scales are K-block-major: Ws[nb, kb] = ws_p[kb * ceil(N / bn) + nb]
+  const bool per_tensor = block_n == 0 && block_k == 0;
+  const int64_t nbn = per_tensor || block_n <= 0 ? 1 : cdiv(N, block_n);
+  const mxq_status vst =
+      validate_mm(A, a_dtype, M, K, lda, a_scale, sa0, sa1, Wp, N, cdiv(K, 16) * 16, ws_p,
+                  block_n, block_k, 1, nbn, bias, bias_dtype, out, out_dtype, ldo);
+  if (vst != MXQ_OK) return vst;
+  if (M == 0 || N == 0) return MXQ_OK;
+  if ((reinterpret_cast<uintptr_t>(Wp) & 255) != 0)
+    return fail(MXQ_ERR_INVALID_ARG, "prepacked weights must be 256-byte aligned");
+  return scaled_mm_run(A, a_dtype, M, K, lda, a_scale, sa0, sa1, nullptr, N, 0,
+                       reinterpret_cast<const uint8_t*>(Wp), ws_p, block_n, block_k, 1, nbn, bias,
+                       bias_dtype, out, out_dtype, ldo, workspace, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------- moe_align

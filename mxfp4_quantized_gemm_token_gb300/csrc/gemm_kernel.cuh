@@ -103,6 +103,11 @@ struct GemmParams {
   int out_dtype;
   int64_t ldo;
   float* partial;
+  // prepacked weights (dense GEMM only), or NULL: 128 x 128-byte tiles, tile
+  // (row block, K slice) at ((row / 128) * nkb + kb) * 16384, each the
+  // 128-byte-swizzled shared-memory image; rows up to npad exist
+  const uint8_t* wpacked;
+  int npad;
   int* status;
   unsigned long long budget_ns;
   int inject_stall;
@@ -141,7 +146,6 @@ struct Layout {
   // output staging of the weight-major epilogue (the token-major one stores directly)
   static constexpr int OUT_BYTES = (EPI == EPI_NORMAL) ? 0 : EW * STG * 128 * 4;
   static constexpr int SSLOTS = 8;                         // scale ring depth
-  static constexpr int NSTR = 160;    // token-major scale slot: 128 As + BT/128 Ws (floats)
   static constexpr int MISC_BYTES = 16384;
   static constexpr int BUDGET = 225 * 1024 - 1024;   // minus alignment slack
   static constexpr int FIXED = OUT_BYTES + MISC_BYTES;
@@ -165,7 +169,7 @@ struct Layout {
   static_assert(AS >= 2 && BS >= 2, "pipeline too shallow");
   static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory over budget");
   static_assert(COLS % 32 == 0 && COLS <= 128, "epilogue column split");
-  static_assert(SSLOTS * NSTR * 4 <= 8192 && SSLOTS * BT * 4 <= 8192, "scale ring size");
+  static_assert(SSLOTS * BT * 4 <= 8192, "scale ring size");
 };
 
 struct Unit {
@@ -381,7 +385,10 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&maps.a);
+  // (maps.a holds the weights in the weight-major orientation; prepacked
+  // weights are read without a tensor map)
+  if (warp == 0 && lane == 0 && (EPI == EPI_NORMAL || p.wpacked == nullptr))
+    tma_prefetch_desc(&maps.a);
   if (warp == 1) {
     tmem_alloc(tmem_slot, L::TMEM_COLS);
     tmem_relinquish();
@@ -412,14 +419,37 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           if (!mbar_wait(&a_empty[s], ((it / AS) & 1) ^ 1, wc)) goto prod_a_done;
           const int kc = (KIND == KIND_MXW) ? kb * 64 : kb * 128;
           uint8_t* dst = sA + s * L::A_BYTES;
-          if (KIND == KIND_F8F8) {
+          if (EPI == EPI_NORMAL && p.wpacked != nullptr) {
+            // token-major with prepacked weights: the B operand (BT weight
+            // rows of slice kb) is BT / 64 contiguous 8 KB halves of packed
+            // tiles; halves past the padded row count are not loaded (their
+            // accumulator columns are never stored)
+            uint32_t bytes = L::A_BYTES;
+#pragma unroll
+            for (int c = 0; c < BT / 64; ++c)
+              if (U.brow + 64 * c < p.npad) bytes += 8192;
+            mbar_expect_tx(&a_full[s], bytes);
+#pragma unroll
+            for (int c = 0; c < BT / 64; ++c) {
+              const int row = U.brow + 64 * c;
+              if (row < p.npad)
+                bulk_load(sB + s * L::B_BYTES + c * 8192,
+                          p.wpacked + (static_cast<int64_t>(row >> 7) * p.nkb + kb) * 16384 +
+                              ((row >> 6) & 1) * 8192,
+                          8192, &a_full[s]);
+            }
+          } else if (KIND == KIND_F8F8) {
             // FP8 x FP8: both operands of the slice land on one barrier
             mbar_expect_tx(&a_full[s], L::A_BYTES + U.brows * 128);
             tma_load_2d(sB + s * L::B_BYTES, &maps.b[U.bvar], &a_full[s], kb * 128, U.brow);
           } else {
             mbar_expect_tx(&a_full[s], L::A_BYTES);
           }
-          if (EPI == EPI_SILU) {
+          if (EPI != EPI_NORMAL && EPI != EPI_SILU && p.wpacked != nullptr) {
+            // weight-major with prepacked weights: one contiguous 16 KB tile
+            bulk_load_hint(dst, p.wpacked + (static_cast<int64_t>(U.wrow0 >> 7) * p.nkb + kb) * 16384,
+                           16384, &a_full[s], pol);
+          } else if (EPI == EPI_SILU) {
             tma_load_2d_hint(dst, &maps.a, &a_full[s], kc, U.wrow0, pol);
             tma_load_2d_hint(dst + L::A_BYTES / 2, &maps.a, &a_full[s], kc, U.wrow1, pol);
           } else {
@@ -634,52 +664,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       }
     mx_done:;
     } else if (EPI == EPI_NORMAL) {
-      // token-major: per slice, As(m, kb) of the tile's 128 token rows and
-      // Ws(blk, kb) of its BT / 128 weight blocks, four slices ahead
-      constexpr int NWB = (BT + 127) / 128 + (BT % 128 != 0 ? 1 : 0);   // weight blocks a tile can span
-      uint32_t is = 0;
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const Unit U = get_unit<EPI, BT>(p, u);
-        float ra[4][4], rw[4];
-        auto fetch = [&](int kb, float* a, float& w) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = lane + 32 * i;
-            a[i] = (r < U.rows)
-                       ? __ldg(p.a_scale + static_cast<int64_t>(U.m0 + r) * p.sa0 + kb * p.sa1)
-                       : 1.f;
-          }
-          w = 1.f;
-          if (lane < NWB) {
-            const int n = (U.n0 / 128 + lane) * 128;
-            if (p.block_n == 0)
-              w = __ldg(p.w_scale);
-            else if (n < p.N)
-              w = __ldg(p.w_scale + static_cast<int64_t>(n / 128) * p.sw0 + kb * p.sw1);
-          }
-        };
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (U.kb0 + q < U.kb1) fetch(U.kb0 + q, ra[q], rw[q]);
-        for (int kb = U.kb0; kb < U.kb1; kb += 4) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (kb + q < U.kb1) {
-              const int slot = is % SSL;
-              if (!mbar_wait(&s_empty[slot], ((is / SSL) & 1) ^ 1, wc)) goto nscale_done;
-              float* dst = sAsc + slot * L::NSTR;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = ra[q][i];
-              if (lane < NWB) dst[128 + lane] = rw[q];
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&s_full[slot]);
-              ++is;
-              if (kb + q + 4 < U.kb1) fetch(kb + q + 4, ra[q], rw[q]);
-            }
-          }
-        }
-      }
-    nscale_done:;
+      // token-major: the epilogue threads read their own slice scales
     } else if (PROMOTE) {
       // Four slices of look-ahead in registers hide the global-load latency.
       constexpr int NA = BT / 32;
@@ -849,31 +834,47 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   } else if (warp >= 4 && EPI == EPI_NORMAL) {
     // ------------------------------------- epilogue, tokens on TMEM lanes
     // Thread = token row m; its slice scale As(m, kb) * Ws(blk, kb) is one
-    // scalar, so promotion is one packed FMA per pair of accumulators.
+    // scalar (a warpgroup's 64 columns lie in one 128-row weight block), so
+    // promotion is one packed FMA per pair of accumulators.  The thread reads
+    // its own scales, so no wait on another warp sits in the slice loop.
     const int g = (warp - 4) >> 2;
     const int et = (threadIdx.x - 128) & 127;
     const int col0 = g * COLS;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t au = 0, is = 0;
+    uint32_t au = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit U = get_unit<EPI, BT>(p, u);
       const bool mrow = et < U.rows;
       const int ncv = min(BT, p.N - U.n0);              // valid weight columns of the tile
       const int colv = max(0, min(COLS, ncv - col0));
       const int ngr = (colv + GRP - 1) / GRP;
-      // weight block of this WG's 64 columns (64-aligned, so inside one block)
-      const int wsel = (U.n0 + col0) / 128 - U.n0 / 128;
       float acc[COLS];
 #pragma unroll
       for (int j = 0; j < COLS; ++j) acc[j] = 0.f;
-      for (int kb = U.kb0; kb < U.kb1; ++kb) {
-        // slice scale As(m, kb) * Ws(blk, kb), staged by the scale loader
-        const int slot = is % SSL;
-        if (!mbar_wait(&s_full[slot], (is / SSL) & 1, wc)) goto epin_done;
-        const float sc = sAsc[slot * L::NSTR + et] * sAsc[slot * L::NSTR + 128 + wsel];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[slot]);
-        ++is;
+      // slice scales: this thread's token row As(m, kb) and its columns'
+      // weight block Ws(blk, kb), read from global memory (L1) four slices
+      // ahead; rows and blocks past the tile's valid ones read a valid entry
+      const float* arow = p.a_scale + static_cast<int64_t>(U.m0 + min(et, U.rows - 1)) * p.sa0;
+      const int wb = min((U.n0 + col0) / 128, (p.N - 1) / 128);
+      const float* wrow = p.w_scale + (p.block_n == 0 ? 0 : static_cast<int64_t>(wb) * p.sw0);
+      const int64_t wk = p.block_n == 0 ? 0 : p.sw1;
+      float ra[4], rw[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int k = min(U.kb0 + q, U.kb1 - 1);
+        ra[q] = __ldg(arow + k * p.sa1);
+        rw[q] = __ldg(wrow + k * wk);
+      }
+      for (int kb4 = U.kb0; kb4 < U.kb1; kb4 += 4)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int kb = kb4 + q;
+        if (kb >= U.kb1) break;
+        const float sc = ra[q] * rw[q];
+        if (kb + 4 < U.kb1) {
+          ra[q] = __ldg(arow + (kb + 4) * p.sa1);
+          rw[q] = __ldg(wrow + (kb + 4) * wk);
+        }
         const uint32_t buf = au % NB;
         if (!mbar_wait(&t_full[buf], (au / NB) & 1, wc)) goto epin_done;
         tc_fence_after();

@@ -118,6 +118,37 @@ def test_workspace_query_and_noalloc_validate_before_any_device_work(lib):
         assert b"scratch" not in lib.mxq_last_error()
 
 
+def test_prepack_argument_errors(lib):
+    """The prepack size query and the prepack refuse what the GEMM refuses,
+    and bad pointers, before any device work."""
+    from mxfp4_quantized_gemm_token_gb300 import _lib
+    wb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    q = lib.mxq_prepacked_weight_size
+    assert q(300, 200, 128, 128, ctypes.byref(wb), ctypes.byref(sb)) == _lib.OK
+    assert wb.value == 3 * 2 * 16384 and sb.value == 3 * 2 * 4
+    assert q(300, 200, 1, 128, ctypes.byref(wb), ctypes.byref(sb)) == _lib.OK
+    assert sb.value == 300 * 2 * 4
+    assert q(300, 200, 0, 0, ctypes.byref(wb), ctypes.byref(sb)) == _lib.OK and sb.value == 4
+    assert q(300, 200, 1, 32, ctypes.byref(wb), ctypes.byref(sb)) == _lib.ERR_UNSUPPORTED
+    assert q(300, 0, 128, 128, ctypes.byref(wb), ctypes.byref(sb)) == _lib.ERR_INVALID_ARG
+    pk = lib.mxq_prepack_weight
+    ALIGNED = ctypes.c_void_p(1 << 20)
+    assert pk(None, 256, 256, 256, FAKE, 128, 128, 2, 1, ALIGNED, FAKE, None) == _lib.ERR_INVALID_ARG
+    assert pk(FAKE, 256, 256, 256, FAKE, 64, 128, 2, 1, ALIGNED, FAKE, None) == _lib.ERR_UNSUPPORTED
+    assert pk(FAKE, 256, 256, 200, FAKE, 128, 128, 2, 1, ALIGNED, FAKE, None) == _lib.ERR_UNSUPPORTED
+    assert pk(FAKE, 256, 256, 256, FAKE, 128, 128, 2, 1, ctypes.c_void_p((1 << 20) + 16), FAKE,
+              None) == _lib.ERR_INVALID_ARG                       # tiles not 256-byte aligned
+    mmp = lib.mxq_fp8_scaled_mm_prepacked
+    args = [FAKE, 3, 4, 256, 256, FAKE, 2, 1, ALIGNED, 128, FAKE, 128, 128, None, 0, FAKE, 1, 128,
+            None, 0, None]
+    bad = list(args)
+    bad[11], bad[12] = 1, 32                                      # MXFP8 [1, 32]
+    assert mmp(*bad) == _lib.ERR_UNSUPPORTED
+    bad = list(args)
+    bad[8] = ctypes.c_void_p((1 << 20) + 16)                      # tiles not 256-byte aligned
+    assert mmp(*bad) == _lib.ERR_INVALID_ARG
+
+
 def test_quant_align_moe_argument_errors(lib):
     from mxfp4_quantized_gemm_token_gb300 import _lib
     q = lib.mxq_per_token_group_quant_fp8

@@ -63,7 +63,7 @@ class Cta:
     """State and roles of one persistent CTA processing `units` (slice counts)."""
 
     def __init__(self, units, promote, ndg, mxw, AS=12, BS=4, CS=4, SSL=8, NB=4,
-                 old_issuer_rule=False, warps_per_group=2, f8f8=False):
+                 old_issuer_rule=False, warps_per_group=2, f8f8=False, scale_ring=True):
         # f8f8: FP8 x FP8 (dense and token-major W8A8): one producer loads both
         # operands of a slice into the A ring, which the MMA issuers read
         # directly; the scale ring feeds the promotion epilogue; no decode
@@ -72,8 +72,9 @@ class Cta:
             promote, ndg, mxw = True, 0, False
         self.units, self.promote, self.ndg, self.mxw = units, promote, ndg, mxw
         # the scale ring feeds the decode (MXFP4) or the promotion epilogue
-        # (promoted kinds); per-tensor whole-K has none
-        self.epi_scales = promote
+        # (promoted kinds); per-tensor whole-K has none, and the token-major
+        # epilogue reads its scales itself (scale_ring=False)
+        self.epi_scales = promote and scale_ring
         self.AS, self.BS, self.CS, self.SSL, self.NB = AS, BS, CS, SSL, NB
         self.old = old_issuer_rule
         self.wpg = warps_per_group
@@ -355,11 +356,15 @@ def test_model_finds_the_stale_read_of_the_per_unit_issuer_rule():
         Cta(UNIT_PATTERNS["odd"], promote=False, ndg=2, mxw=True).run(random.Random(seed))
 
 
-@pytest.mark.parametrize("AS,NB", [(5, 2), (10, 4), (12, 4)])
+@pytest.mark.parametrize("AS,NB,ring", [(6, 4, False), (5, 2, False), (10, 4, True),
+                                        (12, 4, True)])
 @pytest.mark.parametrize("pattern", ["even", "odd", "mixed", "ones"])
-def test_ring_protocol_fp8_x_fp8(AS, NB, pattern):
-    """FP8 x FP8 W8A8: token-major tiles of 192 (5 stages, 2 accumulator
-    buffers) and weight-major decode tiles (10-12 stages, 4 buffers)."""
+def test_ring_protocol_fp8_x_fp8(AS, NB, ring, pattern):
+    """FP8 x FP8 W8A8: token-major tiles of 128 (6 stages, 4 accumulator
+    buffers) and 192 (5 stages, 2 buffers), whose epilogue reads its own slice
+    scales, and weight-major decode tiles (10-12 stages, 4 buffers) fed by the
+    scale ring."""
     for seed in range(40):
-        cta = Cta(UNIT_PATTERNS[pattern], promote=True, ndg=0, mxw=False, AS=AS, NB=NB, f8f8=True)
+        cta = Cta(UNIT_PATTERNS[pattern], promote=True, ndg=0, mxw=False, AS=AS, NB=NB, f8f8=True,
+                  scale_ring=ring)
         cta.run(random.Random(seed))
