@@ -64,11 +64,22 @@ enum {
   MXQ_W_MXFP4 = 2         /* e2m1x2 weights, ue8m0 scale per 32 K elements */
 };
 
+/* stage-1 activations of the fused MoE (gate = rows [0, N) of w1[e], up =
+ * rows [N, 2N)) */
+enum {
+  MXQ_ACT_SILU = 0,         /* act = silu(gate) * up, silu(v) = v / (1 + e^-v) */
+  MXQ_ACT_SWIGLU_CLAMP = 1  /* GPT-OSS-style clamped SwiGLU:
+                               g = min(gate, limit), u = clamp(up, -limit, limit),
+                               act = g / (1 + e^(-alpha g)) * (u + 1) */
+};
+
 /* options (process-wide; mxq_set_option / mxq_get_option) */
 enum {
   MXQ_OPT_SMALL_M_MAX = 1,  /* expert blocks with m_size <= this use the narrowest MMA
                                instruction covering them; larger blocks use the full
-                               block_m width.  Default 1 << 30 (always fit). */
+                               block_m width.  Default 4, the [CPU-MoE] page's small-block
+                               threshold (its tests put 4 on the small path, 5 and 33 on
+                               the large one). */
   MXQ_OPT_FORCE_PATH = 2,   /* 0 per expert block (auto), 1 always narrow (fit), 2 always
                                full width, 3 one path for the whole layer: narrow when
                                max(1, S / E) <= SMALL_M_MAX (the global crossover) */
@@ -81,10 +92,14 @@ enum {
                                256 (256 for FP8 activations only) */
   MXQ_OPT_NORMAL_TILE = 8,  /* fp8_scaled_mm weight-tile width when the tokens sit on
                                the MMA M side (large-M W8A8): 0 auto, 128, 192 or 256 */
-  MXQ_OPT_PDL = 9           /* 1 (default): kernels are launched with programmatic stream
+  MXQ_OPT_PDL = 9,          /* 1 (default): kernels are launched with programmatic stream
                                serialization, so a kernel's launch and prologue overlap the
                                end of the previous kernel on the stream (each waits for it
                                before touching global memory); 0: plain stream order */
+  MXQ_OPT_FUSE_COMBINE = 10 /* fused MoE: 1 (default) the top-k combine runs inside the
+                               stage-2 GEMM (the last of a token's slots to finish a weight
+                               tile sums its rows, ascending k); 0: a separate combine
+                               kernel.  Bit-identical results either way. */
 };
 
 const char* mxq_last_error(void);
@@ -113,6 +128,23 @@ mxq_status mxq_sync_status(mxq_stream_t stream);
 mxq_status mxq_per_token_group_quant_fp8(const void* x, int64_t M, int64_t K, int64_t ldx,
                                          int32_t group, float eps, void* q, float* scales,
                                          mxq_stream_t stream);
+
+/*
+ * Weight quantization to MXFP4 (the expert-weight format of [CPU-MoE]; its
+ * related-PR list names online MXFP4 quantization of the weights), by the OCP
+ * Microscaling (MX) v1.0 rule.  For every block of 32 consecutive values of a
+ * row:
+ *   E = floor(log2(max |v|)) - 2, clamped to [-127, 127]; -127 when all zero
+ *   scales[r, g] = E + 127                      (ue8m0, value 2^E)
+ *   code = E2M1 nearest to v / 2^E, ties to the even code, |.| > 6 -> 6;
+ *          the sign bit is the sign of v (negatives rounding to 0 give -0)
+ *   x       [R, C] MXQ_BF16 or MXQ_F32, row stride ldx; C a multiple of 32
+ *   packed  e2m1x2 [R, C/2] (low nibble = even column), 16-byte aligned
+ *   scales  ue8m0 [R, C/32]
+ * R == 0 is a no-op.
+ */
+mxq_status mxq_quantize_mxfp4(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                              void* packed, void* scales, mxq_stream_t stream);
 
 /*
  * Scaled FP8 GEMM  out[m, n] = sum_k A[m, k] * W[n, k] * scales (+ bias[n]).
@@ -218,6 +250,30 @@ mxq_status mxq_fp8_scaled_mm_prepacked(const void* A, int32_t a_dtype, int64_t M
                                        int64_t ldo, void* workspace, size_t ws_bytes,
                                        mxq_stream_t stream);
 
+/*
+ * Batched scaled FP8 GEMM: `batch` independent mxq_fp8_scaled_mm problems of
+ * one shape in one launch ([CPU-GEMM], motivation: the existing FP8 scaled
+ * GEMM of bmm_cpu serves batched GEMMs such as the DeepSeek MLA projections).
+ * For every b < batch:
+ *   out[b] = scaled_mm(A[b], a_scale[b], W[b], w_scale[b]) (+ bias[b])
+ * with every per-problem argument as in mxq_fp8_scaled_mm, and batch strides
+ * (in elements) between consecutive problems:
+ *   a_bstride   must equal M * lda  (A problems stacked row-contiguously)
+ *   w_bstride   must equal N * ldw  (W problems stacked row-contiguously)
+ *   sa_bstride, sw_bstride, bias_bstride (0 = one bias for all), out_bstride:
+ *               any value >= 0
+ * Other strides give MXQ_ERR_UNSUPPORTED.  No split-K (no workspace).
+ * batch == 0, M == 0 or N == 0 is a no-op.
+ */
+mxq_status mxq_fp8_scaled_bmm(int64_t batch, const void* A, int32_t a_dtype, int64_t M, int64_t K,
+                              int64_t lda, int64_t a_bstride, const float* a_scale, int64_t sa0,
+                              int64_t sa1, int64_t sa_bstride, const void* W, int64_t N,
+                              int64_t ldw, int64_t w_bstride, const float* w_scale,
+                              int32_t block_n, int32_t block_k, int64_t sw0, int64_t sw1,
+                              int64_t sw_bstride, const void* bias, int32_t bias_dtype,
+                              int64_t bias_bstride, void* out, int32_t out_dtype, int64_t ldo,
+                              int64_t out_bstride, mxq_stream_t stream);
+
 /* Workspace bytes of the split-K plan mxq_fp8_scaled_mm runs for this shape
  * on the current device (0 when it does not split).  The plan depends on the
  * activation type and the weight block size (a_dtype, block_n, block_k take
@@ -293,6 +349,20 @@ mxq_status mxq_fused_experts_debug(const void* hidden, int64_t T, int64_t K, int
                                    int32_t topk, int32_t block_m, void* out, int64_t ldo,
                                    void* workspace, size_t ws_bytes, void* act_out,
                                    float* y_out, float* h_out, mxq_stream_t stream);
+
+/* mxq_fused_experts / _debug with a choice of stage-1 activation
+ * (MXQ_ACT_SILU, or MXQ_ACT_SWIGLU_CLAMP with its alpha > 0 and limit > 0;
+ * [CPU-MoE] names GPT-OSS among the MXFP4 MoE models its path serves).  The
+ * checkpoint pointers may be NULL; the workspace is that of
+ * mxq_fused_experts_workspace_size. */
+mxq_status mxq_fused_experts_ex(const void* hidden, int64_t T, int64_t K, int64_t ldh,
+                                int32_t wtype, int32_t E, int64_t N, const void* w1,
+                                const void* w1_scale, const float* w1_bias, const void* w2,
+                                const void* w2_scale, const float* w2_bias,
+                                const float* topk_weights, const int32_t* topk_ids, int32_t topk,
+                                int32_t block_m, int32_t activation, float alpha, float limit,
+                                void* out, int64_t ldo, void* workspace, size_t ws_bytes,
+                                void* act_out, float* y_out, float* h_out, mxq_stream_t stream);
 
 mxq_status mxq_fused_experts_workspace_size(int64_t T, int64_t K, int32_t E, int64_t N,
                                             int32_t topk, int32_t block_m, int32_t wtype,

@@ -23,7 +23,7 @@ from ._lib import MxqError, check
 
 __all__ = [
     "MxqError", "per_token_group_quant_fp8", "fp8_scaled_mm", "w8a8_block_fp8_linear",
-    "PackedWeight", "prepack_weight",
+    "PackedWeight", "prepack_weight", "fp8_scaled_bmm", "quantize_mxfp4",
     "fp8_per_tensor_linear", "moe_align_block", "fused_experts", "align_capacity",
     "set_option", "get_option", "sync_status", "W_FP8_BLOCK128", "W_MXFP4",
 ]
@@ -84,6 +84,23 @@ def per_token_group_quant_fp8(x: torch.Tensor, group: int = 128, eps: float = 1e
     check(_lib_handle().mxq_per_token_group_quant_fp8(
         _ptr(x2), M, K, x2.stride(0), group, float(eps), _ptr(q), _ptr(s), _stream(x.device)))
     return q.view(*x.shape[:-1], K), s.view(*x.shape[:-1], G)
+
+
+def quantize_mxfp4(w: torch.Tensor):
+    """bf16 / fp32 [..., C] (C % 32 == 0) -> (packed e2m1x2 uint8 [..., C/2],
+    ue8m0 uint8 [..., C/32]) by the OCP MX rule."""
+    _need_cuda(w)
+    if w.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("w must be bf16 or fp32")
+    C = w.shape[-1]
+    w2 = _as_rows(w)
+    R = w2.shape[0]
+    packed = torch.empty((R, C // 2), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((R, max(C // 32, 1)), dtype=torch.uint8, device=w.device)
+    check(_lib_handle().mxq_quantize_mxfp4(
+        _ptr(w2), _lib.BF16 if w.dtype == torch.bfloat16 else _lib.F32, R, C, w2.stride(0),
+        _ptr(packed), _ptr(scales), _stream(w.device)))
+    return packed.view(*w.shape[:-1], C // 2), scales.view(*w.shape[:-1], C // 32)
 
 
 # ------------------------------------------------------------- scaled GEMM
@@ -225,6 +242,60 @@ def fp8_scaled_mm(a, w, w_scale, block_size=None, a_scale=None, bias=None,
     return out.view(*a.shape[:-1], N)
 
 
+def fp8_scaled_bmm(a, w, w_scale, block_size=None, a_scale=None, bias=None,
+                   out_dtype=torch.bfloat16):
+    """Batched fp8_scaled_mm: out[b] = scaled_mm(a[b], w[b]) (+ bias[b]).
+
+    a: [B, M, K] e4m3 (with a_scale [B, M, ceil(K/128)]) or bf16; w: e4m3
+    [B, N, K]; w_scale: [B] / [B, 1] (per-tensor) or [B, ceil(N/bn),
+    ceil(K/128)]; bias: None, [N] (shared) or [B, N].  One launch for the
+    whole batch."""
+    _need_cuda(a, w, w_scale, a_scale, bias)
+    lib = _lib_handle()
+    if a.dim() != 3 or w.dim() != 3 or a.shape[0] != w.shape[0] or a.shape[2] != w.shape[2]:
+        raise ValueError("a must be [B, M, K] and w [B, N, K]")
+    a, w = a.contiguous(), w.contiguous()
+    B, M, K = a.shape
+    N = w.shape[1]
+    if a.dtype == torch.float8_e4m3fn:
+        a_dtype = _lib.E4M3
+    elif a.dtype == torch.bfloat16:
+        a_dtype = _lib.BF16
+    else:
+        raise TypeError("a must be float8_e4m3fn or bfloat16")
+    sa0 = sa1 = sab = 0
+    if a_scale is not None:
+        if a_scale.dim() != 3:
+            raise ValueError("a_scale must be [B, M, ceil(K/128)]")
+        sab, sa0, sa1 = a_scale.stride()
+    if block_size is None:
+        bn = bk = 0
+        sw0 = sw1 = 0
+        if w_scale.numel() != B:
+            raise ValueError("per-tensor scales: one per batch")
+        w_scale = w_scale.reshape(B).contiguous()
+        swb = 1
+    else:
+        bn, bk = int(block_size[0]), int(block_size[1])
+        if w_scale.dim() != 3:
+            raise ValueError("block weight scales must be [B, ceil(N/bn), ceil(K/128)]")
+        swb, sw0, sw1 = w_scale.stride()
+    bias_dtype, bb = 0, 0
+    if bias is not None:
+        if bias.dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError("bias must be fp32 or bf16")
+        bias_dtype = _lib.BF16 if bias.dtype == torch.bfloat16 else _lib.F32
+        bias = bias.contiguous()
+        bb = N if bias.dim() == 2 else 0
+    od = _lib.BF16 if out_dtype == torch.bfloat16 else _lib.F32
+    out = torch.empty((B, M, N), dtype=out_dtype, device=a.device)
+    check(lib.mxq_fp8_scaled_bmm(
+        B, _ptr(a), a_dtype, M, K, K, M * K, _ptr(a_scale), sa0, sa1, sab, _ptr(w), N, K, N * K,
+        _ptr(w_scale), bn, bk, sw0, sw1, swb, _ptr(bias), bias_dtype, bb, _ptr(out), od, N, M * N,
+        _stream(a.device)))
+    return out
+
+
 def w8a8_block_fp8_linear(input, weight, block_size, weight_scale, input_scale=None, bias=None):
     """Block-FP8 linear with the pages' semantics: quantize the input per
     1x128 group unless input_scale is given; output bf16 for a pre-quantized
@@ -276,14 +347,20 @@ def moe_align_block(topk_ids: torch.Tensor, num_experts: int, block_m: int, cap=
 
 def fused_experts(hidden, w1, w1_scale, w2, w2_scale, topk_weights, topk_ids,
                   wtype=W_FP8_BLOCK128, w1_bias=None, w2_bias=None, block_m: int = 0,
-                  workspace=None, checkpoints: bool = False):
+                  workspace=None, checkpoints: bool = False, activation: str = "silu",
+                  alpha: float = 1.702, limit: float = 7.0):
     """Routed MoE: align, stage 1 (+ SiLU-and-mul), stage 2, top-k combine.
 
     block_m: tokens per expert block (16, 32, 64, 128), or 0 for the
     library's choice (32 when T*topk <= 16*E, else 64).
     checkpoints: also return, in slot order (t*topk + k), act (bf16 [S, N]),
     y = w * z (fp32 [S, K]) and the stage-1 accumulator h before the bias
-    (fp32 [S, 2N])."""
+    (fp32 [S, 2N]).
+    activation: "silu" (silu(gate) * up) or "swiglu_clamp" (GPT-OSS style:
+    min(gate, limit) * sigmoid(alpha * min(gate, limit)) *
+    (clamp(up, -limit, limit) + 1)); gate = the first N rows of w1[e]."""
+    if activation not in ("silu", "swiglu_clamp"):
+        raise ValueError("activation must be 'silu' or 'swiglu_clamp'")
     _need_cuda(hidden, w1, w1_scale, w2, w2_scale, topk_weights, topk_ids, w1_bias, w2_bias)
     lib = _lib_handle()
     T, K = hidden.shape
@@ -306,6 +383,16 @@ def fused_experts(hidden, w1, w1_scale, w2, w2_scale, topk_weights, topk_ids,
     args = [_ptr(hidden), T, K, hidden.stride(0), wtype, E, N, _ptr(w1), _ptr(w1_scale), _ptr(b1),
             _ptr(w2), _ptr(w2_scale), _ptr(b2), _ptr(tw), _ptr(ids), topk, block_m, _ptr(out), K,
             _ptr(workspace), workspace.numel() * workspace.element_size()]
+    if activation != "silu":
+        act = y = h = None
+        if checkpoints:
+            act = torch.empty((T * topk, N), dtype=torch.bfloat16, device=hidden.device)
+            y = torch.empty((T * topk, K), dtype=torch.float32, device=hidden.device)
+            h = torch.empty((T * topk, 2 * N), dtype=torch.float32, device=hidden.device)
+        check(lib.mxq_fused_experts_ex(*args[:17], _lib.ACT_SWIGLU_CLAMP, float(alpha),
+                                       float(limit), *args[17:], _ptr(act), _ptr(y), _ptr(h),
+                                       _stream(hidden.device)))
+        return (out, act, y, h) if checkpoints else out
     if checkpoints:
         act = torch.empty((T * topk, N), dtype=torch.bfloat16, device=hidden.device)
         y = torch.empty((T * topk, K), dtype=torch.float32, device=hidden.device)

@@ -29,7 +29,7 @@ mxq_status cuda_fail(cudaError_t e, const char* what) {
   return fail(MXQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-std::atomic<int64_t> g_opts[10] = {0, int64_t(1) << 30, 0, 2000000000LL, 0, 0, 0, 0, 0, 1};
+std::atomic<int64_t> g_opts[11] = {0, 4, 0, 2000000000LL, 0, 0, 0, 0, 0, 1, 1};
 
 std::mutex g_dev_mu;
 DeviceInfo g_devs[64];
@@ -135,7 +135,7 @@ extern "C" const char* mxq_last_error(void) { return g_err.c_str(); }
 extern "C" const char* mxq_version(void) { return "mxq 0.1 (sm_103a, tcgen05)"; }
 
 extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
-  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_PDL)
+  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_FUSE_COMBINE)
     return fail(MXQ_ERR_INVALID_ARG, "unknown option " + std::to_string(opt));
   if (opt == MXQ_OPT_NORMAL_TILE && value != 0 && value != 128 && value != 192 && value != 256)
     return fail(MXQ_ERR_INVALID_ARG, "NORMAL_TILE is 0 (auto), 128, 192 or 256");
@@ -143,8 +143,8 @@ extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
       value != 256)
     return fail(MXQ_ERR_INVALID_ARG, "TILE_N is 0 (auto), 32, 64, 128 or 256");
   if (value < 0) return fail(MXQ_ERR_INVALID_ARG, "option values are non-negative");
-  if (opt == MXQ_OPT_PDL && value != 0 && value != 1)
-    return fail(MXQ_ERR_INVALID_ARG, "PDL is 0 (off) or 1 (on)");
+  if ((opt == MXQ_OPT_PDL || opt == MXQ_OPT_FUSE_COMBINE) && value != 0 && value != 1)
+    return fail(MXQ_ERR_INVALID_ARG, "PDL and FUSE_COMBINE are 0 (off) or 1 (on)");
   if (opt == MXQ_OPT_FORCE_PATH && value > 3)
     return fail(MXQ_ERR_INVALID_ARG,
                 "FORCE_PATH is 0 (per block), 1 (narrow), 2 (full width) or 3 (one path per layer)");
@@ -153,7 +153,7 @@ extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
 }
 
 extern "C" mxq_status mxq_get_option(int32_t opt, int64_t* value) {
-  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_PDL || value == nullptr)
+  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_FUSE_COMBINE || value == nullptr)
     return fail(MXQ_ERR_INVALID_ARG, "unknown option or NULL value");
   *value = g_opts[opt].load();
   return MXQ_OK;
@@ -202,6 +202,31 @@ extern "C" mxq_status mxq_per_token_group_quant_fp8(const void* x, int64_t M, in
   cudaError_t e = launch_group_quant(x, M, K, ldx, group, eps, q, scales, d.num_sms,
                                      reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "group quant launch");
+  return MXQ_OK;
+}
+
+// ---------------------------------------------------------- MXFP4 encode
+
+extern "C" mxq_status mxq_quantize_mxfp4(const void* x, int32_t x_dtype, int64_t R, int64_t C,
+                                         int64_t ldx, void* packed, void* scales,
+                                         mxq_stream_t stream) {
+  if (R < 0 || C <= 0) return fail(MXQ_ERR_INVALID_ARG, "need R >= 0 and C > 0");
+  if (C % 32 != 0) return fail(MXQ_ERR_UNSUPPORTED, "C must be a multiple of 32");
+  if (x_dtype != MXQ_BF16 && x_dtype != MXQ_F32)
+    return fail(MXQ_ERR_UNSUPPORTED, "x_dtype must be MXQ_BF16 or MXQ_F32");
+  if (R == 0) return MXQ_OK;
+  if (!x || !packed || !scales) return fail(MXQ_ERR_INVALID_ARG, "NULL tensor argument");
+  if (ldx < C) return fail(MXQ_ERR_INVALID_ARG, "ldx must be >= C");
+  const int es = x_dtype == MXQ_BF16 ? 2 : 4;
+  if (!aligned16(x) || (ldx * es) % 16 != 0 || !aligned16(packed))
+    return fail(MXQ_ERR_UNSUPPORTED,
+                "x and packed need 16-byte aligned bases and x rows a multiple of 16 bytes");
+  DeviceInfo d;
+  std::string err;
+  if (!device_info(&d, &err)) return fail(MXQ_ERR_UNSUPPORTED, err);
+  cudaError_t e = launch_mxfp4_quant(x, x_dtype == MXQ_BF16, R, C, ldx, packed, scales, d.num_sms,
+                                     reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "MXFP4 quantization launch");
   return MXQ_OK;
 }
 
@@ -498,6 +523,100 @@ extern "C" mxq_status mxq_fp8_scaled_mm_prepacked(
                        bias_dtype, out, out_dtype, ldo, workspace, ws_bytes, stream);
 }
 
+extern "C" mxq_status mxq_fp8_scaled_bmm(
+    int64_t batch, const void* A, int32_t a_dtype, int64_t M, int64_t K, int64_t lda,
+    int64_t a_bstride, const float* a_scale, int64_t sa0, int64_t sa1, int64_t sa_bstride,
+    const void* W, int64_t N, int64_t ldw, int64_t w_bstride, const float* w_scale,
+    int32_t block_n, int32_t block_k, int64_t sw0, int64_t sw1, int64_t sw_bstride,
+    const void* bias, int32_t bias_dtype, int64_t bias_bstride, void* out, int32_t out_dtype,
+    int64_t ldo, int64_t out_bstride, mxq_stream_t stream) {
+  if (batch < 0) return fail(MXQ_ERR_INVALID_ARG, "batch must be >= 0");
+  if (batch == 0) return MXQ_OK;
+  const mxq_status vst = validate_mm(A, a_dtype, M, K, lda, a_scale, sa0, sa1, W, N, ldw, w_scale,
+                                     block_n, block_k, sw0, sw1, bias, bias_dtype, out, out_dtype,
+                                     ldo);
+  if (vst != MXQ_OK) return vst;
+  if (M == 0 || N == 0) return MXQ_OK;
+  if (a_bstride != M * lda || w_bstride != N * ldw)
+    return fail(MXQ_ERR_UNSUPPORTED,
+                "A and W batches must be stacked contiguously (a_bstride = M*lda, w_bstride = N*ldw)");
+  if (sa_bstride < 0 || sw_bstride < 0 || bias_bstride < 0 || out_bstride < 0)
+    return fail(MXQ_ERR_INVALID_ARG, "negative batch strides");
+  if (batch * M >= (1LL << 31) || batch * N >= (1LL << 31))
+    return fail(MXQ_ERR_UNSUPPORTED, "batch * M and batch * N must stay below 2^31");
+  const bool per_tensor = block_n == 0 && block_k == 0;
+  DeviceInfo d;
+  std::string err;
+  if (!device_info(&d, &err)) return fail(MXQ_ERR_UNSUPPORTED, err);
+  const int sms = sms_for_grid(d);
+  // weight-major tiles (tokens on the MMA N side), no split-K: the batch
+  // itself provides the parallelism of the small per-head problems
+  MmPlan pl = plan_for_call(M, N, K, a_dtype, block_n, block_k, sms);
+  if (pl.normal) {
+    pl.normal = false;
+    pl.bt = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
+    pl.tiles_n = static_cast<int>(cdiv(N, 128));
+    pl.tiles_m = static_cast<int>(cdiv(M, pl.bt));
+  }
+  pl.splits = 1;
+  pl.kb_per_split = pl.nkb;
+  GemmMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  const int bv = pl.bt == 32 ? 1 : (pl.bt == 64 ? 2 : (pl.bt == 128 ? 3 : 4));
+  if (!make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, K, batch * N, ldw, 128, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B, &err))
+    return fail(MXQ_ERR_CUDA, err);
+  if (a_dtype == MXQ_E4M3) {
+    if (!make_map_2d(&maps.b[bv], CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, batch * M, lda, 128, pl.bt,
+                     CU_TENSOR_MAP_SWIZZLE_128B, &err))
+      return fail(MXQ_ERR_CUDA, err);
+  } else if (!make_map_2d(&maps.b[bv], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, batch * M, lda * 2,
+                          64, pl.bt, CU_TENSOR_MAP_SWIZZLE_128B, &err)) {
+    return fail(MXQ_ERR_CUDA, err);
+  }
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.nkb = pl.nkb;
+  p.tiles_n = pl.tiles_n;
+  p.tiles_m = pl.tiles_m;
+  p.splits = 1;
+  p.kb_per_split = pl.nkb;
+  p.batch = static_cast<int>(batch);
+  p.a_scale = a_scale;
+  p.sa0 = sa0;
+  p.sa1 = sa1;
+  p.sa_e = sa_bstride;
+  p.w_scale = w_scale;
+  p.sw0 = sw0;
+  p.sw1 = sw1;
+  p.sw_e = sw_bstride;
+  p.block_n = per_tensor ? 0 : block_n;
+  p.bias = bias;
+  p.bias_dtype = bias ? bias_dtype : 0;
+  p.bias_e = bias_bstride;
+  p.out = out;
+  p.out_dtype = out_dtype;
+  p.ldo = ldo;
+  p.out_e = out_bstride;
+  p.npad = static_cast<int>(cdiv(N, 128) * 128);
+  p.status = d.status;
+  p.budget_ns = static_cast<unsigned long long>(option(MXQ_OPT_WAIT_BUDGET_NS));
+  p.inject_stall = static_cast<int>(option(MXQ_OPT_INJECT_STALL));
+  const uintptr_t ob = reinterpret_cast<uintptr_t>(out);
+  p.vec_ok = (ldo % 4 == 0) && (out_bstride % 4 == 0) &&
+             ((out_dtype == MXQ_BF16) ? (ob & 7) == 0 : (ob & 15) == 0);
+  const int64_t units = static_cast<int64_t>(pl.tiles_n) * pl.tiles_m * batch;
+  if (units >= (1LL << 31)) return fail(MXQ_ERR_UNSUPPORTED, "too many tiles");
+  const int grid = static_cast<int>(std::min<int64_t>(units, sms));
+  cudaError_t e = launch_gemm(pl.kind, EPI_DENSE, pl.bt, pl.promote, maps, p, grid,
+                              reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "scaled-bmm launch");
+  return MXQ_OK;
+}
+
 // ------------------------------------------------------------- moe_align
 
 extern "C" mxq_status mxq_moe_align_block(const int32_t* topk_ids, int64_t T, int32_t topk,
@@ -534,8 +653,8 @@ extern "C" mxq_status mxq_moe_align_block(const int32_t* topk_ids, int64_t T, in
 namespace {
 
 struct MoeWs {
-  size_t sorted, experts, offsets, nblocks, xs, ic1, y, total;
-  int64_t S, cap;
+  size_t sorted, experts, offsets, nblocks, xs, ic1, y, cnt, total;
+  int64_t S, cap, ncnt;
 };
 
 // block_m 0: the library's choice.  Expert blocks of 32 slots let the
@@ -567,6 +686,10 @@ MoeWs moe_ws(int64_t T, int64_t K, int32_t E, int64_t N, int32_t topk, int32_t b
   o = round_up(o + static_cast<size_t>(w.S) * N * 2, 256);
   w.y = o;
   o = round_up(o + static_cast<size_t>(w.S) * K * 4, 256);
+  // fused combine: one counter per (token, 128-row tile of the K outputs)
+  w.cnt = o;
+  w.ncnt = T * cdiv(K, 128);
+  o = round_up(o + static_cast<size_t>(w.ncnt) * 4, 256);
   w.total = o;
   return w;
 }
@@ -577,7 +700,8 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
                               const float* w2_bias, const float* topk_weights,
                               const int32_t* topk_ids, int32_t topk, int32_t block_m, void* out,
                               int64_t ldo, void* workspace, size_t ws_bytes, void* act_out,
-                              float* y_out, float* h_out, cudaStream_t st) {
+                              float* y_out, float* h_out, int32_t activation, float alpha,
+                              float limit, cudaStream_t st) {
   if (T < 0 || K <= 0 || N <= 0 || topk <= 0)
     return fail(MXQ_ERR_INVALID_ARG, "need T >= 0, K > 0, N > 0, topk > 0");
   if (T == 0) return MXQ_OK;
@@ -585,6 +709,10 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
     return fail(MXQ_ERR_INVALID_ARG, "NULL tensor argument");
   if (E < 1 || E > 1024) return fail(MXQ_ERR_UNSUPPORTED, "E must be in [1, 1024]");
   if (topk > E) return fail(MXQ_ERR_INVALID_ARG, "topk must be <= E");
+  if (activation != MXQ_ACT_SILU && activation != MXQ_ACT_SWIGLU_CLAMP)
+    return fail(MXQ_ERR_UNSUPPORTED, "activation must be MXQ_ACT_SILU or MXQ_ACT_SWIGLU_CLAMP");
+  if (activation == MXQ_ACT_SWIGLU_CLAMP && !(limit > 0.f && alpha > 0.f && alpha < 3.4e38f))
+    return fail(MXQ_ERR_INVALID_ARG, "clamped SwiGLU needs alpha > 0 and limit > 0");
   block_m = resolve_block_m(block_m, T * topk, E);
   if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128)
     return fail(MXQ_ERR_UNSUPPORTED, "block_m must be 0 (library choice), 16, 32, 64 or 128");
@@ -617,11 +745,14 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
   void* xs = ws + w.xs;
   void* ic1 = ws + w.ic1;
   float* y = reinterpret_cast<float*>(ws + w.y);
+  const bool fuse_combine = option(MXQ_OPT_FUSE_COMBINE) != 0;
+  int* cnt = reinterpret_cast<int*>(ws + w.cnt);
 
   cudaError_t e = launch_moe_align(topk_ids, w.S, E, block_m, sorted_ids, expert_ids, offsets,
                                    nblocks, w.cap, d.status, st);
   if (e != cudaSuccess) return cuda_fail(e, "moe_align launch");
-  e = launch_gather_rows(hidden, ldh, K, topk, sorted_ids, offsets, nblocks, block_m, w.cap, xs, st);
+  e = launch_gather_rows(hidden, ldh, K, topk, sorted_ids, offsets, nblocks, block_m, w.cap, xs,
+                         fuse_combine ? cnt : nullptr, w.ncnt, st);
   if (e != cudaSuccess) return cuda_fail(e, "gather launch");
 
   const bool fp8 = wtype == MXQ_W_FP8_BLOCK128;
@@ -686,6 +817,9 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
     p.block_m = block_m;
     p.narrow_max = narrow_max;
     p.n_half = static_cast<int>(N);
+    p.act = activation == MXQ_ACT_SWIGLU_CLAMP ? 1 : 0;
+    p.act_alpha = alpha;
+    p.act_limit = limit;
     if (fp8) {
       p.w_scale = reinterpret_cast<const float*>(wsc);
       p.sw0 = cdiv(red, 128);
@@ -708,6 +842,12 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
     p.bias_e = rows;
     p.route_w = topk_weights;
     p.h_out = stage == 0 ? h_out : nullptr;
+    if (stage == 1 && fuse_combine) {
+      p.combine_cnt = cnt;
+      p.combine_out = out;
+      p.combine_ldo = ldo;
+      p.topk = topk;
+    }
     p.out = stage == 0 ? ic1 : static_cast<void*>(y);
     p.out_dtype = stage == 0 ? MXQ_BF16 : MXQ_F32;
     p.ldo = stage == 0 ? N : K;
@@ -719,8 +859,10 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
     e = launch_gemm(kind, stage == 0 ? EPI_SILU : EPI_SCATTER, bt, fp8, maps, p, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, stage == 0 ? "stage-1 launch" : "stage-2 launch");
   }
-  e = launch_combine(y, T, topk, K, out, ldo, st);
-  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  if (!fuse_combine) {
+    e = launch_combine(y, T, topk, K, out, ldo, st);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  }
   if (act_out) {
     e = launch_unsort_rows(ic1, N, sorted_ids, offsets, nblocks, block_m, w.cap, act_out, st);
     if (e != cudaSuccess) return cuda_fail(e, "unsort launch");
@@ -753,7 +895,7 @@ extern "C" mxq_status mxq_fused_experts(const void* hidden, int64_t T, int64_t K
                                         void* workspace, size_t ws_bytes, mxq_stream_t stream) {
   return fused_experts_impl(hidden, T, K, ldh, wtype, E, N, w1, w1_scale, w1_bias, w2, w2_scale,
                             w2_bias, topk_weights, topk_ids, topk, block_m, out, ldo, workspace,
-                            ws_bytes, nullptr, nullptr, nullptr,
+                            ws_bytes, nullptr, nullptr, nullptr, MXQ_ACT_SILU, 0.f, 0.f,
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -765,5 +907,19 @@ extern "C" mxq_status mxq_fused_experts_debug(
     void* act_out, float* y_out, float* h_out, mxq_stream_t stream) {
   return fused_experts_impl(hidden, T, K, ldh, wtype, E, N, w1, w1_scale, w1_bias, w2, w2_scale,
                             w2_bias, topk_weights, topk_ids, topk, block_m, out, ldo, workspace,
-                            ws_bytes, act_out, y_out, h_out, reinterpret_cast<cudaStream_t>(stream));
+                            ws_bytes, act_out, y_out, h_out, MXQ_ACT_SILU, 0.f, 0.f,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" mxq_status mxq_fused_experts_ex(
+    const void* hidden, int64_t T, int64_t K, int64_t ldh, int32_t wtype, int32_t E, int64_t N,
+    const void* w1, const void* w1_scale, const float* w1_bias, const void* w2,
+    const void* w2_scale, const float* w2_bias, const float* topk_weights, const int32_t* topk_ids,
+    int32_t topk, int32_t block_m, int32_t activation, float alpha, float limit, void* out,
+    int64_t ldo, void* workspace, size_t ws_bytes, void* act_out, float* y_out, float* h_out,
+    mxq_stream_t stream) {
+  return fused_experts_impl(hidden, T, K, ldh, wtype, E, N, w1, w1_scale, w1_bias, w2, w2_scale,
+                            w2_bias, topk_weights, topk_ids, topk, block_m, out, ldo, workspace,
+                            ws_bytes, act_out, y_out, h_out, activation, alpha, limit,
+                            reinterpret_cast<cudaStream_t>(stream));
 }

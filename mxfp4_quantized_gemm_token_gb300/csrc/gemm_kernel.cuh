@@ -74,6 +74,12 @@ struct GemmParams {
   int tiles_m;
   int splits;
   int kb_per_split;
+  // batched dense GEMM (weight-major only): `batch` independent problems of
+  // M x N x K; A and W are stacked along their rows (batch b's rows at
+  // b*M / b*N), scales, bias and output advance by sa_e / sw_e / bias_e /
+  // out_e per batch (the batch index takes the place of the expert)
+  int batch;
+  int64_t sa_e, out_e;
   // grouped (MoE) work description, produced on the device by moe_align
   int grouped;
   const int* num_blocks;
@@ -83,6 +89,8 @@ struct GemmParams {
   int block_m;
   int narrow_max;     // blocks with m_size <= narrow_max use the narrowest legal MMA N
   int n_half;         // SiLU stage: intermediate size N (gate rows = [0, N))
+  int act;            // SiLU stage activation: 0 SiLU-and-mul, 1 clamped SwiGLU
+  float act_alpha, act_limit;
   // scales
   const float* a_scale;
   int64_t sa0, sa1;
@@ -98,6 +106,14 @@ struct GemmParams {
   int bias_dtype;
   int64_t bias_e;
   const float* route_w;
+  // scatter stage, fused top-k combine (or NULL): one counter per (token,
+  // weight tile), zero at entry; the warp that completes a token's tile sums
+  // its topk rows of y in ascending k into combine_out (bf16, row stride
+  // combine_ldo)
+  int* combine_cnt;
+  void* combine_out;
+  int64_t combine_ldo;
+  int topk;
   float* h_out;       // SiLU stage, debug: the fp32 accumulator (before bias) in slot order, or NULL
   void* out;
   int out_dtype;
@@ -197,13 +213,15 @@ __device__ __forceinline__ Unit get_unit(const GemmParams& p, int u) {
   Unit U;
   if (!p.grouped) {
     const int per = p.tiles_m * p.splits;
-    U.tn = u / per;
-    const int r = u - U.tn * per;
+    const int per_b = p.tiles_n * per;
+    U.e = (p.batch > 1) ? u / per_b : 0;
+    const int ub = u - U.e * per_b;
+    U.tn = ub / per;
+    const int r = ub - U.tn * per;
     const int tm = r / p.splits;
     U.split = r - tm * p.splits;
     U.kb0 = U.split * p.kb_per_split;
     U.kb1 = min(p.nkb, U.kb0 + p.kb_per_split);
-    U.e = 0;
     U.blk = 0;
     U.n_inst = BT;
     U.bvar = box_variant(BT);
@@ -220,9 +238,9 @@ __device__ __forceinline__ Unit get_unit(const GemmParams& p, int u) {
       U.n0 = U.tn * 128;
       U.m0 = tm * BT;
       U.rows = min(BT, p.M - U.m0);
-      U.wrow0 = U.n0;
-      U.wrow1 = U.n0;
-      U.brow = U.m0;
+      U.wrow0 = U.e * p.N + U.n0;
+      U.wrow1 = U.wrow0;
+      U.brow = U.e * p.M + U.m0;
     }
   } else {
     U.blk = u / p.tiles_n;
@@ -402,8 +420,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   pdl_wait();
   pdl_launch_dependents();
 
-  const int total =
-      p.grouped ? __ldg(p.num_blocks) * p.tiles_n : p.tiles_n * p.tiles_m * p.splits;
+  const int total = p.grouped ? __ldg(p.num_blocks) * p.tiles_n
+                              : p.tiles_n * p.tiles_m * p.splits * max(1, p.batch);
 
   if (warp == 0) {
     // ------------------------------------------------ weight producer
@@ -677,7 +695,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           for (int i = 0; i < NA; ++i) {
             const int j = lane + 32 * i;
             a[i] = (p.a_scale != nullptr && j < U.rows)
-                       ? __ldg(p.a_scale + static_cast<int64_t>(U.m0 + j) * p.sa0 + kb * p.sa1)
+                       ? __ldg(p.a_scale + U.e * p.sa_e + static_cast<int64_t>(U.m0 + j) * p.sa0 +
+                               kb * p.sa1)
                        : 1.f;
           }
           if (lane_ws) {
@@ -690,7 +709,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
             uni = 1.f;
           } else {
             uni = (p.block_n == 0)
-                      ? __ldg(p.w_scale)
+                      ? __ldg(p.w_scale + U.e * p.sw_e)
                       : __ldg(p.w_scale + U.e * p.sw_e + (U.n0 / p.block_n) * p.sw0 + kb * p.sw1);
           }
         };
@@ -1037,7 +1056,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           ++is;
         }
       } else {
-        if (p.block_n == 0 && p.w_scale != nullptr) fscale = __ldg(p.w_scale);
+        if (p.block_n == 0 && p.w_scale != nullptr) fscale = __ldg(p.w_scale + U.e * p.sw_e);
         // the unit's two accumulators (one per MMA issuer); the second is
         // unwritten when the unit has a single K slice
         const uint32_t tb0 = 2 * au, tb1 = 2 * au + 1;
@@ -1107,7 +1126,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
                 } else {
 #pragma unroll
                   for (int i = 0; i < 4; ++i) vv[i] += b4[i];
-                  const int64_t o = static_cast<int64_t>(m) * p.ldo + n;
+                  const int64_t o = U.e * p.out_e + static_cast<int64_t>(m) * p.ldo + n;
                   if (p.out_dtype == DT_BF16) {
                     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
                     if (p.vec_ok && n + 3 < p.N) {
@@ -1147,9 +1166,18 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
                     hr[U.n0 + l] = stg[jj * 128 + l];
                     hr[p.n_half + U.n0 + l] = stg[jj * 128 + 64 + l];
                   }
-                  const float gt = stg[jj * 128 + l] + bias_g;
-                  const float up = stg[jj * 128 + 64 + l] + bias_u;
-                  const float a = gt / (1.0f + expf(-gt)) * up;
+                  float gt = stg[jj * 128 + l] + bias_g;
+                  float up = stg[jj * 128 + 64 + l] + bias_u;
+                  float a;
+                  if (p.act == 0) {
+                    a = gt / (1.0f + expf(-gt)) * up;
+                  } else {
+                    // clamped SwiGLU: gate <= limit, |up| <= limit,
+                    // gate * sigmoid(alpha * gate) * (up + 1)
+                    gt = fminf(gt, p.act_limit);
+                    up = fminf(fmaxf(up, -p.act_limit), p.act_limit);
+                    a = gt / (1.0f + expf(-p.act_alpha * gt)) * (up + 1.0f);
+                  }
                   reinterpret_cast<__nv_bfloat16*>(p.out)[static_cast<int64_t>(U.m0 + col) * p.ldo +
                                                           U.n0 + l] = __float2bfloat16_rn(a);
                 }
@@ -1167,6 +1195,36 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                   if (n + i < p.N) dst[n + i] = (vv[i] + b4[i]) * rw;
+                if (p.combine_cnt != nullptr) {
+                  // the last of the token's topk slots to reach this tile
+                  // sums them (release: fence before the count; acquire: fence
+                  // after seeing the others' counts)
+                  const int t = slot / p.topk;
+                  __syncwarp();
+                  int last = 0;
+                  if (lane == 0) {
+                    __threadfence();
+                    last = atomicAdd(p.combine_cnt + static_cast<int64_t>(t) * p.tiles_n + U.tn, 1) ==
+                           p.topk - 1;
+                    if (last) __threadfence();
+                  }
+                  last = __shfl_sync(0xffffffffu, last, 0);
+                  if (last) {
+                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int k = 0; k < p.topk; ++k) {
+                      const float* yr = reinterpret_cast<const float*>(p.out) +
+                                        (static_cast<int64_t>(t) * p.topk + k) * p.ldo;
+#pragma unroll
+                      for (int i = 0; i < 4; ++i)
+                        if (n + i < p.N) s4[i] += __ldcg(yr + n + i);
+                    }
+                    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.combine_out) +
+                                       static_cast<int64_t>(t) * p.combine_ldo;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                      if (n + i < p.N) o[n + i] = __float2bfloat16_rn(s4[i]);
+                  }
+                }
               }
             }
             if (!group_sync(&epi_bar[g], eph, wc)) goto epi_done;

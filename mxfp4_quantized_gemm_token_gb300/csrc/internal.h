@@ -79,6 +79,9 @@ cudaError_t launch_gemm(int kind, int epi, int bt, bool promote, const GemmMaps&
 cudaError_t launch_group_quant(const void* x, int64_t M, int64_t K, int64_t ldx, int group,
                                float eps, void* q, float* scales, int num_sms, cudaStream_t stream);
 
+cudaError_t launch_mxfp4_quant(const void* x, bool bf16, int64_t R, int64_t C, int64_t ldx,
+                               void* packed, void* scales, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_moe_align(const int32_t* topk_ids, int64_t S, int32_t E, int32_t block_m,
                              int32_t* sorted_ids, int32_t* expert_ids, int32_t* offsets,
                              int32_t* num_blocks, int64_t cap, int* status, cudaStream_t stream);
@@ -86,7 +89,7 @@ cudaError_t launch_moe_align(const int32_t* topk_ids, int64_t S, int32_t E, int3
 cudaError_t launch_gather_rows(const void* hidden, int64_t ldh, int64_t K, int32_t topk,
                                const int32_t* sorted_ids, const int32_t* offsets,
                                const int32_t* num_blocks, int32_t block_m, int64_t cap, void* xs,
-                               cudaStream_t stream);
+                               int* zero, int64_t nzero, cudaStream_t stream);
 
 cudaError_t launch_combine(const float* y, int64_t T, int32_t topk, int64_t K, void* out,
                            int64_t ldo, cudaStream_t stream);

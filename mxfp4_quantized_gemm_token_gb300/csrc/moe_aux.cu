@@ -181,9 +181,14 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int
                                    int topk, const int32_t* __restrict__ sorted_ids,
                                    const int32_t* __restrict__ offsets,
                                    const int32_t* __restrict__ num_blocks, int BM,
-                                   __nv_bfloat16* __restrict__ xs, int vec) {
+                                   __nv_bfloat16* __restrict__ xs, int vec, int* __restrict__ zero,
+                                   int64_t nzero) {
   pdl_wait();
   pdl_launch_dependents();
+  // also clears the fused combine's counters for this call
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nzero;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    zero[i] = 0;
   const int nb = __ldg(num_blocks);
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -208,7 +213,7 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int
 cudaError_t launch_gather_rows(const void* hidden, int64_t ldh, int64_t K, int32_t topk,
                                const int32_t* sorted_ids, const int32_t* offsets,
                                const int32_t* num_blocks, int32_t block_m, int64_t cap, void* xs,
-                               cudaStream_t stream) {
+                               int* zero, int64_t nzero, cudaStream_t stream) {
   const int vec = (K % 8 == 0) && (ldh % 8 == 0) &&
                   (reinterpret_cast<uintptr_t>(hidden) & 15) == 0 &&
                   (reinterpret_cast<uintptr_t>(xs) & 15) == 0;
@@ -218,7 +223,8 @@ cudaError_t launch_gather_rows(const void* hidden, int64_t ldh, int64_t K, int32
   if (blocks < 1) blocks = 1;
   return launch_k(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
                   reinterpret_cast<const __nv_bfloat16*>(hidden), ldh, K, topk, sorted_ids,
-                  offsets, num_blocks, block_m, reinterpret_cast<__nv_bfloat16*>(xs), vec);
+                  offsets, num_blocks, block_m, reinterpret_cast<__nv_bfloat16*>(xs), vec, zero,
+                  zero != nullptr ? nzero : 0);
 }
 
 // ------------------------------------------------------------ combine

@@ -181,3 +181,96 @@ cudaError_t launch_group_quant(const void* x, int64_t M, int64_t K, int64_t ldx,
 }
 
 }  // namespace mxq
+
+// ------------------------------------------------------------ MXFP4 encode
+// Weight quantization to MXFP4 by the OCP Microscaling (MX) v1.0 rule, the
+// format of the MXFP4 expert weights ("[CPU] routed FP8/MXFP4 MoE", related
+// PR 49347: online MXFP4 quantization).  Per block of 32 consecutive values:
+// shared exponent E = floor(log2(amax)) - 2 clamped to [-127, 127] (-127 for
+// an all-zero block), ue8m0 byte E + 127, elements = E2M1 round-to-nearest-
+// even of v * 2^-E with saturation at 6 (the conversion instruction's rule),
+// sign kept.  One thread per block: 64 (bf16) or 128 (fp32) contiguous bytes
+// in, 16 bytes of codes and one scale byte out.
+namespace mxq {
+
+__device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <bool BF16IN>
+__global__ void mxfp4_quant_kernel(const void* __restrict__ x, int64_t R, int64_t C, int64_t ldx,
+                                   uint8_t* __restrict__ packed, uint8_t* __restrict__ scales) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t G = C / 32;
+  const int64_t total = R * G;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / G, g = i - r * G;
+    float v[32];
+    if (BF16IN) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(x) + r * ldx + g * 32);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 w = __ldg(src + j);
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          v[8 * j + 2 * t] = __uint_as_float(wv[t] << 16);
+          v[8 * j + 2 * t + 1] = __uint_as_float(wv[t] & 0xFFFF0000u);
+        }
+      }
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) +
+                                                          r * ldx + g * 32);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 w = __ldg(src + j);
+        v[4 * j] = w.x;
+        v[4 * j + 1] = w.y;
+        v[4 * j + 2] = w.z;
+        v[4 * j + 3] = w.w;
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    int E = -127;
+    if (amax > 0.f) E = max(-127, min(127, ilogbf(amax) - 2));
+    const float inv = ldexpf(1.0f, -E);   // 2^-E: exact (2^127 down to 2^-127)
+    uint32_t words[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        w |= e2m1x2_rn(v[8 * j + 2 * t] * inv, v[8 * j + 2 * t + 1] * inv) << (8 * t);
+      words[j] = w;
+    }
+    *reinterpret_cast<uint4*>(packed + r * (C / 2) + g * 16) =
+        make_uint4(words[0], words[1], words[2], words[3]);
+    scales[r * G + g] = static_cast<uint8_t>(E + 127);
+  }
+}
+
+cudaError_t launch_mxfp4_quant(const void* x, bool bf16, int64_t R, int64_t C, int64_t ldx,
+                               void* packed, void* scales, int num_sms, cudaStream_t stream) {
+  const int64_t total = R * (C / 32);
+  int64_t blocks = (total + 127) / 128;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (bf16)
+    return launch_k(mxfp4_quant_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(128), 0,
+                    stream, x, R, C, ldx, reinterpret_cast<uint8_t*>(packed),
+                    reinterpret_cast<uint8_t*>(scales));
+  return launch_k(mxfp4_quant_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(128), 0,
+                  stream, x, R, C, ldx, reinterpret_cast<uint8_t*>(packed),
+                  reinterpret_cast<uint8_t*>(scales));
+}
+
+}  // namespace mxq

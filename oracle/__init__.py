@@ -90,6 +90,12 @@ def _load():
                                              P, P, P, P, P, I32, P, I64, P, P]
         lib.oracle_expert_linear.restype = None
         lib.oracle_expert_linear.argtypes = [P, I64, I64, I32, P, P, I64, I64, I64, P]
+        lib.oracle_mxfp4_quantize.restype = None
+        lib.oracle_mxfp4_quantize.argtypes = [P, I64, I64, I64, P, P]
+        lib.oracle_fused_experts_act.restype = I32
+        lib.oracle_fused_experts_act.argtypes = [P, I64, I64, I64, I32, I32, I64, P, P, P,
+                                                 P, P, P, P, P, I32, I32, ctypes.c_double,
+                                                 ctypes.c_double, P, I64, P, P]
         lib.oracle_max_threads.restype = I32
         lib.oracle_set_threads.argtypes = [I32]
         _lib = lib
@@ -255,8 +261,10 @@ def moe_align(topk_ids, E: int, block_m: int, cap: int | None = None):
 
 
 def fused_experts(hidden_bits, wtype, w1, w1_scale, b1, w2, w2_scale, b2,
-                  topk_weights, topk_ids, N: int, checkpoints: bool = False):
-    """Reference routed MoE.  Returns out bf16 bits [T, K] (and act, z)."""
+                  topk_weights, topk_ids, N: int, checkpoints: bool = False,
+                  activation: int = 0, alpha: float = 1.702, limit: float = 7.0):
+    """Reference routed MoE.  Returns out bf16 bits [T, K] (and act, z).
+    activation 0: SiLU-and-mul; 1: clamped SwiGLU (alpha, limit)."""
     lib = _load()
     x = _c(hidden_bits, np.uint16)
     T, K = x.shape
@@ -277,9 +285,10 @@ def fused_experts(hidden_bits, wtype, w1, w1_scale, b1, w2, w2_scale, b2,
     out = np.empty((T, K), dtype=np.uint16)
     act = np.empty((T * topk, N), dtype=np.uint16) if checkpoints else None
     z = np.empty((T * topk, K), dtype=np.float64) if checkpoints else None
-    rc = lib.oracle_fused_experts(_ptr(x), T, K, K, wtype, E, N, _ptr(w1), _ptr(w1_scale),
-                                  _ptr(b1), _ptr(w2), _ptr(w2_scale), _ptr(b2), _ptr(tw),
-                                  _ptr(ids), topk, _ptr(out), K, _ptr(act), _ptr(z))
+    rc = lib.oracle_fused_experts_act(_ptr(x), T, K, K, wtype, E, N, _ptr(w1), _ptr(w1_scale),
+                                      _ptr(b1), _ptr(w2), _ptr(w2_scale), _ptr(b2), _ptr(tw),
+                                      _ptr(ids), topk, int(activation), float(alpha),
+                                      float(limit), _ptr(out), K, _ptr(act), _ptr(z))
     if rc != 0:
         raise ValueError("oracle_fused_experts failed with code %d" % rc)
     if checkpoints:
@@ -303,6 +312,20 @@ def expert_linear(x_bits, wtype, w, w_scale, e: int):
     out = np.empty((M, R), dtype=np.float64)
     lib.oracle_expert_linear(_ptr(x), M, C, wtype, _ptr(w), _ptr(w_scale), e, R, C, _ptr(out))
     return out
+
+
+def mxfp4_quantize(x_f32):
+    """OCP MX rule: fp32 [R, C] (C % 32 == 0) -> (packed e2m1 [R, C/2] uint8,
+    ue8m0 scales [R, C/32] uint8)."""
+    lib = _load()
+    x = _c(np.asarray(x_f32, dtype=np.float32), np.float32)
+    R, C = x.shape
+    if C % 32 != 0:
+        raise ValueError("C must be a multiple of 32")
+    packed = np.zeros((R, C // 2), dtype=np.uint8)
+    scales = np.empty((R, C // 32), dtype=np.uint8)
+    lib.oracle_mxfp4_quantize(_ptr(x), R, C, C, _ptr(packed), _ptr(scales))
+    return packed, scales
 
 
 def max_threads() -> int:

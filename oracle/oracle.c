@@ -406,13 +406,30 @@ void oracle_expert_linear(const uint16_t* x, int64_t M, int64_t ldx, int32_t wty
  * b2 [E, K] fp32 or NULL; out bf16 [T, K] row stride ldo.  act_out (bf16
  * [T*topk, N]) and z_out (fp64 [T*topk, K]) are optional checkpoints in
  * slot order.  Returns -2 if an id is out of range. */
-int32_t oracle_fused_experts(const uint16_t* hidden, int64_t T, int64_t K, int64_t ldh,
-                             int32_t wtype, int32_t E, int64_t N,
-                             const void* w1, const void* w1_scale, const float* b1,
-                             const void* w2, const void* w2_scale, const float* b2,
-                             const float* topk_weights, const int32_t* topk_ids,
-                             int32_t topk, uint16_t* out, int64_t ldo,
-                             uint16_t* act_out, double* z_out) {
+/* The stage-1 activation of the fused MoE on one pair (gate g, up u):
+ *   kind 0, SiLU-and-mul ([vLLM-50949] "activation" between the stages):
+ *       silu(g) * u with silu(v) = v / (1 + e^-v)
+ *   kind 1, GPT-OSS-style clamped SwiGLU (GPT-OSS is among the MXFP4 models
+ *       [vLLM-50949] serves): g' = min(g, limit), u' = clamp(u, -limit, limit),
+ *       g' / (1 + e^(-alpha g')) * (u' + 1)
+ * evaluated in fp64. */
+static double moe_activation(int32_t kind, double alpha, double limit, double g, double u) {
+  if (kind == 1) {
+    if (g > limit) g = limit;
+    if (u > limit) u = limit;
+    if (u < -limit) u = -limit;
+    return g / (1.0 + exp(-alpha * g)) * (u + 1.0);
+  }
+  return g / (1.0 + exp(-g)) * u;
+}
+
+int32_t oracle_fused_experts_act(const uint16_t* hidden, int64_t T, int64_t K, int64_t ldh,
+                                 int32_t wtype, int32_t E, int64_t N,
+                                 const void* w1, const void* w1_scale, const float* b1,
+                                 const void* w2, const void* w2_scale, const float* b2,
+                                 const float* topk_weights, const int32_t* topk_ids,
+                                 int32_t topk, int32_t act_kind, double alpha, double limit,
+                                 uint16_t* out, int64_t ldo, uint16_t* act_out, double* z_out) {
   for (int64_t i = 0; i < T * topk; ++i)
     if (topk_ids[i] < 0 || topk_ids[i] >= E) return -2;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -431,9 +448,7 @@ int32_t oracle_fused_experts(const uint16_t* hidden, int64_t T, int64_t K, int64
         if (b1) h[r] += (double)b1[e * 2 * N + r];
       }
       for (int64_t i = 0; i < N; ++i) {
-        double g = h[i];
-        double silu = g / (1.0 + exp(-g));
-        uint16_t a16 = oracle_bf16_round(silu * h[N + i]);
+        uint16_t a16 = oracle_bf16_round(moe_activation(act_kind, alpha, limit, h[i], h[N + i]));
         act[i] = oracle_bf16_decode(a16);
         if (act_out) act_out[slot * N + i] = a16;
       }
@@ -448,6 +463,76 @@ int32_t oracle_fused_experts(const uint16_t* hidden, int64_t T, int64_t K, int64
     free(x); free(h); free(act); free(z); free(o);
   }
   return 0;
+}
+
+/* The fused MoE with the SiLU-and-mul activation. */
+int32_t oracle_fused_experts(const uint16_t* hidden, int64_t T, int64_t K, int64_t ldh,
+                             int32_t wtype, int32_t E, int64_t N,
+                             const void* w1, const void* w1_scale, const float* b1,
+                             const void* w2, const void* w2_scale, const float* b2,
+                             const float* topk_weights, const int32_t* topk_ids,
+                             int32_t topk, uint16_t* out, int64_t ldo,
+                             uint16_t* act_out, double* z_out) {
+  return oracle_fused_experts_act(hidden, T, K, ldh, wtype, E, N, w1, w1_scale, b1, w2, w2_scale,
+                                  b2, topk_weights, topk_ids, topk, 0, 0.0, 0.0, out, ldo,
+                                  act_out, z_out);
+}
+
+/* ------------------------------------------------------ MXFP4 quantizer */
+
+/* Conversion of fp32 values to MXFP4 by the OCP Microscaling (MX) v1.0 rule,
+ * the format of the MXFP4 expert weights of [vLLM-50949] (its related PR
+ * 49347 quantizes weights to MXFP4 online).  Per block of 32 consecutive
+ * values of a row:
+ *   E = floor(log2(max |v|)) - 2  (2 = largest exponent of E2M1), clamped to
+ *       [-127, 127]; an all-zero block takes E = -127;
+ *   scale byte = E + 127 (ue8m0, value 2^E);
+ *   each element = the E2M1 value nearest to v / 2^E (searched over the 8
+ *       magnitudes), ties to the code with an even last bit, magnitudes above
+ *       6 saturated to 6; the sign bit copies the sign of v, so negative
+ *       values that round to zero give -0 (code 8).
+ * x fp32 [R, C] row stride ldx, C a multiple of 32; packed [R, C/2] (low
+ * nibble = even column); scales [R, C/32]. */
+void oracle_mxfp4_quantize(const float* x, int64_t R, int64_t C, int64_t ldx, uint8_t* packed,
+                           uint8_t* scales) {
+  static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  for (int64_t r = 0; r < R; ++r) {
+    for (int64_t g = 0; g < C / 32; ++g) {
+      const float* v = x + r * ldx + g * 32;
+      double amax = 0.0;
+      for (int i = 0; i < 32; ++i)
+        if (fabs((double)v[i]) > amax) amax = fabs((double)v[i]);
+      int E = -127;
+      if (amax > 0.0) {
+        int e2;
+        (void)frexp(amax, &e2);  /* amax = f * 2^e2 with f in [0.5, 1) */
+        E = (e2 - 1) - 2;
+        if (E < -127) E = -127;
+        if (E > 127) E = 127;
+      }
+      scales[r * (C / 32) + g] = (uint8_t)(E + 127);
+      for (int i = 0; i < 32; ++i) {
+        double t = ldexp((double)v[i], -E);
+        double a = fabs(t);
+        int best = 7;
+        if (a < 6.0) {
+          best = 0;
+          for (int c = 1; c < 8; ++c) {
+            double dc = fabs(a - mag[c]), db = fabs(a - mag[best]);
+            if (dc < db || (dc == db && (c & 1) == 0)) best = c;
+          }
+        }
+        uint8_t nib = (uint8_t)best;
+        if (signbit(t)) nib |= 8;
+        int64_t col = g * 32 + i;
+        uint8_t* dst = packed + r * (C / 2) + col / 2;
+        if (col % 2 == 0)
+          *dst = (uint8_t)((*dst & 0xF0) | nib);
+        else
+          *dst = (uint8_t)((*dst & 0x0F) | (nib << 4));
+      }
+    }
+  }
 }
 
 /* ------------------------------------------------------------- threading */

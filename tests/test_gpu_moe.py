@@ -64,18 +64,19 @@ def weights(wtype, E, N, K, seed, bias):
 
 
 def run_moe(oracle, wtype, E, N, K, x, tw, ids, block_m, seed=1, bias=False, check_ckpt=True,
-            wts=None):
+            wts=None, activation="silu", alpha=1.702, limit=7.0):
     w1, s1, w2, s2, b1, b2 = weights(wtype, E, N, K, seed, bias) if wts is None else wts
     sc = (lambda s: u8(s)) if wtype == W_MX else (lambda s: s.numpy())
     ref, ract, rz = oracle.fused_experts(
         bits16(x), wtype, u8(w1), sc(s1), None if b1 is None else b1.numpy(), u8(w2), sc(s2),
-        None if b2 is None else b2.numpy(), tw.numpy(), ids.numpy(), N, checkpoints=True)
+        None if b2 is None else b2.numpy(), tw.numpy(), ids.numpy(), N, checkpoints=True,
+        activation=0 if activation == "silu" else 1, alpha=alpha, limit=limit)
     cu = lambda t: None if t is None else t.cuda()
+    kw = dict(wtype=wtype, w1_bias=cu(b1), w2_bias=cu(b2), block_m=block_m,
+              activation=activation, alpha=alpha, limit=limit)
     out, act, y, h = mxq.fused_experts(cu(x), cu(w1), cu(s1), cu(w2), cu(s2), cu(tw), cu(ids),
-                                       wtype=wtype, w1_bias=cu(b1), w2_bias=cu(b2),
-                                       block_m=block_m, checkpoints=True)
-    plain = mxq.fused_experts(cu(x), cu(w1), cu(s1), cu(w2), cu(s2), cu(tw), cu(ids),
-                              wtype=wtype, w1_bias=cu(b1), w2_bias=cu(b2), block_m=block_m)
+                                       checkpoints=True, **kw)
+    plain = mxq.fused_experts(cu(x), cu(w1), cu(s1), cu(w2), cu(s2), cu(tw), cu(ids), **kw)
     mxq.sync_status()
     assert torch.equal(plain, out)          # the checkpoints do not change the result
     assert_bf16_close(out, ref, what="moe output")
@@ -184,3 +185,36 @@ def test_fused_mxfp4_scales_beyond_bf16_single_step(oracle):
     x = synth.activations(T, K, seed=53, scale_div=10)
     tw, ids = synth.routing_uniform(T, E, topk, seed=54)
     run_moe(oracle, W_MX, E, N, K, x, tw, ids, 16, wts=(w1, s1, w2, s2, b1, b2))
+
+
+@pytest.mark.parametrize("wtype", [W_FP8, W_MX])
+@pytest.mark.parametrize("limit", [7.0, 0.05])
+def test_fused_clamped_swiglu(oracle, wtype, limit):
+    """GPT-OSS-style clamped SwiGLU between the stages, with a limit the
+    stage-1 values stay under (7) and one that clamps most of them (0.05),
+    both weight formats, biases, topk 4."""
+    E, N, K, T, topk = 6, 160, 288, 11, 4
+    x = synth.activations(T, K, seed=81, scale_div=10)
+    tw, ids = synth.routing_uniform(T, E, topk, seed=82)
+    run_moe(oracle, wtype, E, N, K, x, tw, ids, 16, bias=True, activation="swiglu_clamp",
+            alpha=1.702, limit=limit)
+
+
+@pytest.mark.parametrize("wtype,T,topk,E", [(W_FP8, 37, 8, 32), (W_MX, 50, 4, 16),
+                                            (W_FP8, 5, 2, 3)])
+def test_fused_combine_is_bit_identical_to_the_combine_kernel(oracle, wtype, T, topk, E):
+    """The top-k combine inside the stage-2 GEMM (default) and the separate
+    combine kernel give the same bits (same fp32 adds, ascending k), and
+    agree with the oracle."""
+    N, K = 128, 384
+    x = synth.activations(T, K, seed=T, scale_div=10)
+    tw, ids = synth.routing_zipf(T, E, topk, seed=T + 1)
+    outs = []
+    try:
+        for fuse in (1, 0):
+            mxq.set_option(_lib.OPT_FUSE_COMBINE, fuse)
+            outs.append(run_moe(oracle, wtype, E, N, K, x, tw, ids, 16, bias=(wtype == W_MX),
+                                check_ckpt=False))
+    finally:
+        mxq.set_option(_lib.OPT_FUSE_COMBINE, 1)
+    assert torch.equal(outs[0], outs[1])
