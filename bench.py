@@ -622,6 +622,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mxq", choices=["mxq", "reference"])
+    ap.add_argument("--opt", action="append", default=[],
+                    help="library option OPTION=VALUE (MXQ_OPT_* number), repeatable")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8-peak", action="store_true",
                     help="measure the vendor FP8 GEMM burst rate (8192^3) and exit")
@@ -641,6 +643,11 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.opt:
+        import mxfp4_quantized_gemm_token_gb300 as mxq
+        for kv in args.opt:
+            k, v = kv.split("=")
+            mxq.set_option(int(k), int(v))
     if args.profile:
         return run_profile(args, local)
     if args.fp8_peak:

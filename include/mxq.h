@@ -96,10 +96,22 @@ enum {
                                serialization, so a kernel's launch and prologue overlap the
                                end of the previous kernel on the stream (each waits for it
                                before touching global memory); 0: plain stream order */
-  MXQ_OPT_FUSE_COMBINE = 10 /* fused MoE: 1 (default) the top-k combine runs inside the
-                               stage-2 GEMM (the last of a token's slots to finish a weight
-                               tile sums its rows, ascending k); 0: a separate combine
-                               kernel.  Bit-identical results either way. */
+  MXQ_OPT_FUSE_COMBINE = 10, /* fused MoE: 1 the top-k combine runs inside the stage-2
+                               GEMM (the last of a token's slots to finish a weight tile sums
+                               its rows, ascending k); 0 (default, measured faster on GB300):
+                               a separate combine kernel.  Bit-identical results either way. */
+  MXQ_OPT_MOE_F16 = 11      /* fused MoE operand type: 1 (default) f16 for FP8-block experts,
+                               bf16 for MXFP4; 2 f16 for both; 0 bf16 for both.  With f16 the
+                               expert GEMMs multiply f16 operands:
+                               weights decode to f16 in one conversion per pair (MXFP4
+                               groups scaled by 2^(e - emax of their 128-wide slice), the
+                               slice's 2^(emax-127) applied per row in fp32), and token
+                               rows are converted to f16 after a power-of-two row scaling
+                               that the epilogue undoes; 0: bf16 operands (weights decoded
+                               to bf16, tokens as given).  The f16 operands are exact
+                               except for elements more than ~2^31 below their token row's
+                               maximum and MXFP4 groups more than 2^23 below the largest
+                               group scale of their slice. */
 };
 
 const char* mxq_last_error(void);

@@ -21,7 +21,8 @@ BF16, F32, E4M3, E2M1X2, UE8M0 = 1, 2, 3, 4, 5
 W_FP8_BLOCK128, W_MXFP4 = 1, 2
 ACT_SILU, ACT_SWIGLU_CLAMP = 0, 1
 (OPT_SMALL_M_MAX, OPT_FORCE_PATH, OPT_WAIT_BUDGET_NS, OPT_SPLIT_K, OPT_INJECT_STALL, OPT_NUM_SMS,
- OPT_TILE_N, OPT_NORMAL_TILE, OPT_PDL, OPT_FUSE_COMBINE) = (1, 2, 3, 4, 5, 6, 7, 8, 9, 10)
+ OPT_TILE_N, OPT_NORMAL_TILE, OPT_PDL, OPT_FUSE_COMBINE, OPT_MOE_F16) = (1, 2, 3, 4, 5, 6, 7, 8, 9, 10,
+                                                                   11)
 
 EXPORTED = [
     "mxq_last_error", "mxq_version", "mxq_set_option", "mxq_get_option", "mxq_sync_status",

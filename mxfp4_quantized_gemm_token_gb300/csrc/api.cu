@@ -29,7 +29,7 @@ mxq_status cuda_fail(cudaError_t e, const char* what) {
   return fail(MXQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-std::atomic<int64_t> g_opts[11] = {0, 4, 0, 2000000000LL, 0, 0, 0, 0, 0, 1, 1};
+std::atomic<int64_t> g_opts[12] = {0, 4, 0, 2000000000LL, 0, 0, 0, 0, 0, 1, 0, 1};
 
 std::mutex g_dev_mu;
 DeviceInfo g_devs[64];
@@ -135,7 +135,7 @@ extern "C" const char* mxq_last_error(void) { return g_err.c_str(); }
 extern "C" const char* mxq_version(void) { return "mxq 0.1 (sm_103a, tcgen05)"; }
 
 extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
-  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_FUSE_COMBINE)
+  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_MOE_F16)
     return fail(MXQ_ERR_INVALID_ARG, "unknown option " + std::to_string(opt));
   if (opt == MXQ_OPT_NORMAL_TILE && value != 0 && value != 128 && value != 192 && value != 256)
     return fail(MXQ_ERR_INVALID_ARG, "NORMAL_TILE is 0 (auto), 128, 192 or 256");
@@ -145,6 +145,8 @@ extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
   if (value < 0) return fail(MXQ_ERR_INVALID_ARG, "option values are non-negative");
   if ((opt == MXQ_OPT_PDL || opt == MXQ_OPT_FUSE_COMBINE) && value != 0 && value != 1)
     return fail(MXQ_ERR_INVALID_ARG, "PDL and FUSE_COMBINE are 0 (off) or 1 (on)");
+  if (opt == MXQ_OPT_MOE_F16 && value > 2)
+    return fail(MXQ_ERR_INVALID_ARG, "MOE_F16 is 0, 1 or 2");
   if (opt == MXQ_OPT_FORCE_PATH && value > 3)
     return fail(MXQ_ERR_INVALID_ARG,
                 "FORCE_PATH is 0 (per block), 1 (narrow), 2 (full width) or 3 (one path per layer)");
@@ -153,7 +155,7 @@ extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
 }
 
 extern "C" mxq_status mxq_get_option(int32_t opt, int64_t* value) {
-  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_FUSE_COMBINE || value == nullptr)
+  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_MOE_F16 || value == nullptr)
     return fail(MXQ_ERR_INVALID_ARG, "unknown option or NULL value");
   *value = g_opts[opt].load();
   return MXQ_OK;
@@ -653,7 +655,7 @@ extern "C" mxq_status mxq_moe_align_block(const int32_t* topk_ids, int64_t T, in
 namespace {
 
 struct MoeWs {
-  size_t sorted, experts, offsets, nblocks, xs, ic1, y, cnt, total;
+  size_t sorted, experts, offsets, nblocks, xs, ic1, y, cnt, hf16, tscale, rs1, ic1h, rs2, total;
   int64_t S, cap, ncnt;
 };
 
@@ -690,6 +692,18 @@ MoeWs moe_ws(int64_t T, int64_t K, int32_t E, int64_t N, int32_t topk, int32_t b
   w.cnt = o;
   w.ncnt = T * cdiv(K, 128);
   o = round_up(o + static_cast<size_t>(w.ncnt) * 4, 256);
+  // f16 operands: the token rows, their scales, the compact rows' scales, the
+  // stage-2 input and its row scales
+  w.hf16 = o;
+  o = round_up(o + static_cast<size_t>(T) * K * 2, 256);
+  w.tscale = o;
+  o = round_up(o + static_cast<size_t>(T) * 4, 256);
+  w.rs1 = o;
+  o = round_up(o + static_cast<size_t>(w.S) * 4, 256);
+  w.ic1h = o;
+  o = round_up(o + static_cast<size_t>(w.S) * N * 2, 256);
+  w.rs2 = o;
+  o = round_up(o + static_cast<size_t>(w.S) * 4, 256);
   w.total = o;
   return w;
 }
@@ -747,16 +761,28 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
   float* y = reinterpret_cast<float*>(ws + w.y);
   const bool fuse_combine = option(MXQ_OPT_FUSE_COMBINE) != 0;
   int* cnt = reinterpret_cast<int*>(ws + w.cnt);
+  const int64_t f16_opt = option(MXQ_OPT_MOE_F16);
+  const bool f16 = f16_opt == 2 || (f16_opt == 1 && wtype == MXQ_W_FP8_BLOCK128);
+  void* hf16 = ws + w.hf16;
+  float* tscale = reinterpret_cast<float*>(ws + w.tscale);
+  float* rs1 = reinterpret_cast<float*>(ws + w.rs1);
+  void* ic1h = ws + w.ic1h;
+  float* rs2 = reinterpret_cast<float*>(ws + w.rs2);
 
   cudaError_t e = launch_moe_align(topk_ids, w.S, E, block_m, sorted_ids, expert_ids, offsets,
                                    nblocks, w.cap, d.status, st);
   if (e != cudaSuccess) return cuda_fail(e, "moe_align launch");
-  e = launch_gather_rows(hidden, ldh, K, topk, sorted_ids, offsets, nblocks, block_m, w.cap, xs,
-                         fuse_combine ? cnt : nullptr, w.ncnt, st);
+  if (f16) {
+    e = launch_rows_to_f16(hidden, T, K, ldh, nullptr, hf16, tscale, st);
+    if (e != cudaSuccess) return cuda_fail(e, "token conversion launch");
+  }
+  e = launch_gather_rows(f16 ? hf16 : hidden, f16 ? K : ldh, K, topk, sorted_ids, offsets, nblocks,
+                         block_m, w.cap, xs, fuse_combine ? cnt : nullptr, w.ncnt,
+                         f16 ? tscale : nullptr, f16 ? rs1 : nullptr, st);
   if (e != cudaSuccess) return cuda_fail(e, "gather launch");
 
   const bool fp8 = wtype == MXQ_W_FP8_BLOCK128;
-  const int kind = fp8 ? KIND_F8W : KIND_MXW;
+  const int kind = fp8 ? (f16 ? KIND_F8H : KIND_F8W) : (f16 ? KIND_MXH : KIND_MXW);
   const int bt = std::max(32, static_cast<int>(block_m));
   const int64_t force = option(MXQ_OPT_FORCE_PATH);
   const int64_t small_m = std::min<int64_t>(option(MXQ_OPT_SMALL_M_MAX), 1 << 30);
@@ -777,7 +803,12 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
     const int64_t red = stage == 0 ? K : N;        // reduction length
     const void* wt = stage == 0 ? w1 : w2;
     const void* wsc = stage == 0 ? w1_scale : w2_scale;
-    const void* src = stage == 0 ? xs : ic1;
+    if (stage == 1 && f16) {
+      // stage-2 tokens: the act rows (bf16) as f16 with their row scales
+      e = launch_rows_to_f16(ic1, w.S, N, N, nullptr, ic1h, rs2, st);
+      if (e != cudaSuccess) return cuda_fail(e, "act conversion launch");
+    }
+    const void* src = stage == 0 ? xs : (f16 ? ic1h : ic1);
     GemmMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     const uint32_t arows = stage == 0 ? 64 : 128;
@@ -795,8 +826,9 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
     for (int v = 0; v < 4; ++v) {
       const uint32_t br = 16u << v;
       if (static_cast<int>(br) > bt) break;
-      if (!make_map_2d(&maps.b[v], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src, red, w.S, red * 2, 64,
-                       br, CU_TENSOR_MAP_SWIZZLE_128B, &err))
+      if (!make_map_2d(&maps.b[v],
+                       f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src,
+                       red, w.S, red * 2, 64, br, CU_TENSOR_MAP_SWIZZLE_128B, &err))
         return fail(MXQ_ERR_CUDA, err);
     }
     GemmParams p;
@@ -837,6 +869,12 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
       }
       p.block_n = 0;
     }
+    if (f16) {
+      // column scales: the inverse power of two of each compact token row
+      p.a_scale = stage == 0 ? rs1 : rs2;
+      p.sa0 = 1;
+      p.sa1 = 0;
+    }
     p.bias = stage == 0 ? w1_bias : w2_bias;
     p.bias_dtype = MXQ_F32;
     p.bias_e = rows;
@@ -851,12 +889,14 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
     p.out = stage == 0 ? ic1 : static_cast<void*>(y);
     p.out_dtype = stage == 0 ? MXQ_BF16 : MXQ_F32;
     p.ldo = stage == 0 ? N : K;
+    // scatter: 16-byte y rows (the workspace is 256-byte aligned)
+    p.vec_ok = stage == 1 && K % 4 == 0;
     p.status = d.status;
     p.budget_ns = static_cast<unsigned long long>(option(MXQ_OPT_WAIT_BUDGET_NS));
     p.inject_stall = static_cast<int>(option(MXQ_OPT_INJECT_STALL));
     const int64_t units = w.cap * p.tiles_n;
     const int grid = static_cast<int>(std::min<int64_t>(units, sms));
-    e = launch_gemm(kind, stage == 0 ? EPI_SILU : EPI_SCATTER, bt, fp8, maps, p, grid, st);
+    e = launch_gemm(kind, stage == 0 ? EPI_SILU : EPI_SCATTER, bt, fp8 || f16, maps, p, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, stage == 0 ? "stage-1 launch" : "stage-2 launch");
   }
   if (!fuse_combine) {

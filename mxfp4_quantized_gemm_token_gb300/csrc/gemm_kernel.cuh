@@ -52,7 +52,16 @@
 
 namespace mxq {
 
-enum { KIND_F8F8 = 0, KIND_F8W = 1, KIND_MXW = 2 };
+// KIND_F8W / KIND_MXW: e4m3 / e2m1 weights decoded to bf16, bf16 tokens.
+// KIND_F8H / KIND_MXH (the fused MoE): the same weights decoded to f16, one
+// conversion instruction per pair; the tokens are f16 rows pre-scaled by a
+// power of two whose inverse is the column scale.  MXH decodes each 32-group
+// as e2m1 * 2^(e - emax) with emax the largest ue8m0 exponent of the row's
+// 128-wide slice; 2^(emax - 127) is the row's promotion factor of the slice.
+enum { KIND_F8F8 = 0, KIND_F8W = 1, KIND_MXW = 2, KIND_F8H = 3, KIND_MXH = 4 };
+__host__ __device__ constexpr bool kind_mx(int k) { return k == KIND_MXW || k == KIND_MXH; }
+__host__ __device__ constexpr bool kind_f8w(int k) { return k == KIND_F8W || k == KIND_F8H; }
+__host__ __device__ constexpr bool kind_f16(int k) { return k == KIND_F8H || k == KIND_MXH; }
 // EPI_DENSE: weights on the MMA M side (swap-AB; decode and [1,128] blocks)
 // EPI_NORMAL: tokens on the MMA M side, weights on N (large M with uniform
 //             [128,128] / per-tensor weight scales: the slice scale is one
@@ -143,10 +152,13 @@ struct Layout {
   // one group's decode is latency-bound (its integer ALU work leaves the
   // pipe half idle)
   static constexpr int NDG =
-      ((KIND == KIND_MXW && BT <= 64) || (KIND == KIND_F8W && BT <= 32)) ? 2 : 1;
+      ((KIND == KIND_MXW && BT <= 64) || (KIND == KIND_MXH && BT <= 32) ||
+       (kind_f8w(KIND) && BT <= 32))
+          ? 2
+          : 1;
   static constexpr int NCV = (KIND == KIND_F8F8) ? 0 : 8 * NDG;
   static constexpr int kThreads = 128 * (1 + EW) + 32 * NCV;
-  static constexpr int A_BYTES = (KIND == KIND_MXW) ? 128 * 64 : 128 * 128;
+  static constexpr int A_BYTES = kind_mx(KIND) ? 128 * 64 : 128 * 128;
   static constexpr int B_BYTES = BT * 128 * ((KIND == KIND_F8F8) ? 1 : 2);
   // bf16 kinds: decoded weight slices (128 rows x 128 K bf16 = 64 TMEM
   // columns each) live in a TMEM ring and feed the MMA's A operand directly
@@ -186,6 +198,7 @@ struct Layout {
   static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory over budget");
   static_assert(COLS % 32 == 0 && COLS <= 128, "epilogue column split");
   static_assert(SSLOTS * BT * 4 <= 8192, "scale ring size");
+  static_assert(KIND != KIND_MXH || SSLOTS * BT * 4 <= 4096, "f16 MXFP4 column scales and bytes overlap");
 };
 
 struct Unit {
@@ -325,6 +338,35 @@ __device__ __forceinline__ void e2m1x8_to_bf16x8(uint32_t word, uint32_t k2, uin
   o[3] = f16x2_bits_to_bf16x2(h3, k2);
 }
 
+// f16 decode (KIND_F8H / KIND_MXH): e4m3 and e2m1 values are exact f16, so
+// the conversion instruction's result is the operand; MXFP4 multiplies each
+// pair by the group's f16 factor 2^(e - emax) (exact while e - emax >= -23).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t word, uint32_t& lo, uint32_t& hi) {
+  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.rn.f16x2.e4m3x2 %0, a; cvt.rn.f16x2.e4m3x2 %1, b; }"
+      : "=r"(lo), "=r"(hi) : "r"(word));
+}
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t word, uint32_t f2, uint32_t* o) {
+  uint32_t h[4];
+  asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;"
+      " cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;"
+      " cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(word));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h[i]), *reinterpret_cast<const __half2*>(&f2));
+    o[i] = *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+// f16 bits of 2^d for d <= 0 (subnormal below 2^-14, zero below 2^-24)
+__device__ __forceinline__ uint32_t f16_pow2(int d) {
+  return d >= -14 ? static_cast<uint32_t>(d + 15) << 10 : (d >= -24 ? 1u << (d + 24) : 0u);
+}
+// largest byte of a 32-bit word
+__device__ __forceinline__ uint32_t max_byte(uint32_t w) {
+  const uint32_t m = __vmaxu4(w, w >> 16);
+  return __vmaxu4(m, m >> 8) & 0xFFu;
+}
+
 // Barrier of the 128 epilogue threads on an mbarrier, so that it is bounded
 // like every other wait (a plain bar.sync would hang if one warp gave up).
 __device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, const WaitCtx& w) {
@@ -367,14 +409,16 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* sAsc = reinterpret_cast<float*>(misc + 1024);            // [SSL][BT] column scales
   float* sWr = reinterpret_cast<float*>(misc + 1024 + 8192);      // [SSL][128] row scales
-  // MXFP4: [SSL][128] ue8m0 bytes of one slice, 4 per weight row (shares sAsc)
-  uint32_t* sMx = reinterpret_cast<uint32_t*>(misc + 1024);
+  // MXFP4: [SSL][128] ue8m0 bytes of one slice, 4 per weight row (shares
+  // sAsc for bf16 decode; its own area for f16 decode, whose slots also
+  // carry column scales, BT <= 128)
+  uint32_t* sMx = reinterpret_cast<uint32_t*>(misc + 1024 + (KIND == KIND_MXH ? 4096 : 0));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   WaitCtx wc{p.status, abort_flag, p.budget_ns};
   // a row scale per TMEM lane is needed when Ws is not uniform over the tile
-  const bool lane_ws = PROMOTE && (p.block_n == 1 || EPI == EPI_SILU);
+  const bool lane_ws = PROMOTE && (p.block_n == 1 || EPI == EPI_SILU || KIND == KIND_MXH);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < AS; ++i) {
@@ -395,7 +439,9 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     }
     for (int i = 0; i < SSL; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], KIND == KIND_MXW ? 8 : 4 * EW);
+      // MXFP4 slots feed one decode group (bf16) or a decode group and the
+      // epilogue (f16, per-slice promotion)
+      mbar_init(&s_empty[i], KIND == KIND_MXW ? 8 : (KIND == KIND_MXH ? 8 + 4 * EW : 4 * EW));
     }
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
@@ -435,7 +481,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
           const int s = it % AS;
           if (!mbar_wait(&a_empty[s], ((it / AS) & 1) ^ 1, wc)) goto prod_a_done;
-          const int kc = (KIND == KIND_MXW) ? kb * 64 : kb * 128;
+          const int kc = kind_mx(KIND) ? kb * 64 : kb * 128;
           uint8_t* dst = sA + s * L::A_BYTES;
           if (EPI == EPI_NORMAL && p.wpacked != nullptr) {
             // token-major with prepacked weights: the B operand (BT weight
@@ -534,7 +580,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         const int brows = U.brows;
         const int nsl = U.kb1 - U.kb0;
         const uint32_t idesc =
-            (KIND == KIND_F8F8) ? idesc_e4m3(128, U.n_inst) : idesc_bf16(128, U.n_inst);
+            (KIND == KIND_F8F8) ? idesc_e4m3(128, U.n_inst)
+                                : (kind_f16(KIND) ? idesc_f16(128, U.n_inst) : idesc_bf16(128, U.n_inst));
         uint32_t ubuf = 0;
         if (!PROMOTE) {
           const uint32_t tb = 2 * au + mine;
@@ -681,6 +728,72 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         }
       }
     mx_done:;
+    } else if (KIND == KIND_MXH) {
+      // MXFP4 decoded to f16, promoted per slice: each slot carries the
+      // slice's ue8m0 bytes (4 per weight row; past K: 0, the data there is
+      // zero), the row's factor 2^(emax - 127) and the column (token) scales
+      constexpr int MLA = 4;
+      constexpr int NA = BT / 32;
+      uint32_t is = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit U = get_unit<EPI, BT>(p, u);
+        float ta[NA];
+#pragma unroll
+        for (int i = 0; i < NA; ++i) {
+          const int j = lane + 32 * i;
+          ta[i] = (p.a_scale != nullptr && j < U.rows) ? __ldg(p.a_scale + U.m0 + j) : 1.f;
+        }
+        uint32_t rb[MLA][4];
+        auto fetch = [&](int kb, uint32_t* b) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = lane + 32 * i;
+            int64_t grow = (EPI == EPI_SILU) ? static_cast<int64_t>(r < 64 ? U.wrow0 + r : U.wrow1 + (r - 64))
+                                             : static_cast<int64_t>(U.wrow0) + r;
+            if (grow >= p.mx_rows_total) grow = p.mx_rows_total - 1;
+            const uint8_t* rowp = p.mx_scale + grow * p.mx_ld + kb * 4;
+            if (p.mx_align >= 4 && kb * 4 + 4 <= p.mx_cols) {
+              b[i] = __ldg(reinterpret_cast<const uint32_t*>(rowp));
+            } else if (p.mx_align >= 2 && kb * 4 + 4 <= p.mx_cols) {
+              const uint16_t* hp = reinterpret_cast<const uint16_t*>(rowp);
+              b[i] = static_cast<uint32_t>(__ldg(hp)) | (static_cast<uint32_t>(__ldg(hp + 1)) << 16);
+            } else {
+              uint32_t v = 0;
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                if (kb * 4 + c < p.mx_cols) v |= static_cast<uint32_t>(__ldg(rowp + c)) << (8 * c);
+              b[i] = v;
+            }
+          }
+        };
+#pragma unroll
+        for (int q = 0; q < MLA; ++q)
+          if (U.kb0 + q < U.kb1) fetch(U.kb0 + q, rb[q]);
+        for (int kb = U.kb0; kb < U.kb1; kb += MLA) {
+#pragma unroll
+          for (int q = 0; q < MLA; ++q) {
+            if (kb + q < U.kb1) {
+              const int slot = is % SSL;
+              if (!mbar_wait(&s_empty[slot], ((is / SSL) & 1) ^ 1, wc)) goto mxh_done;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int r = lane + 32 * i;
+                sMx[slot * 128 + r] = rb[q][i];
+                const uint32_t emax = max_byte(rb[q][i]);
+                // 2^(emax - 127) in fp32 (2^-127 is the subnormal 0x00400000)
+                sWr[slot * 128 + r] = __uint_as_float(emax != 0 ? emax << 23 : 0x00400000u);
+              }
+#pragma unroll
+              for (int i = 0; i < NA; ++i) sAsc[slot * BT + lane + 32 * i] = ta[i];
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&s_full[slot]);
+              ++is;
+              if (kb + q + MLA < U.kb1) fetch(kb + q + MLA, rb[q]);
+            }
+          }
+        }
+      }
+    mxh_done:;
     } else if (EPI == EPI_NORMAL) {
       // token-major: the epilogue threads read their own slice scales
     } else if (PROMOTE) {
@@ -761,7 +874,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         const Unit U = get_unit<EPI, BT>(p, u);
         for (int kb = U.kb0; kb < U.kb1; ++kb, ++ia, ++ic) {
           if (L::NDG > 1 && ia % L::NDG != grp) {
-            if (KIND == KIND_MXW) ++is;   // the other group's scale slot
+            if (kind_mx(KIND)) ++is;   // the other group's scale slot
             continue;
           }
           const int sa = ia % AS, sc = ic % CS;
@@ -770,7 +883,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           tc_fence_after();
           const uint8_t* src = sA + sa * L::A_BYTES;
           uint32_t w[32];
-          if (KIND == KIND_F8W) {
+          if (kind_f8w(KIND)) {
             // 64 fp8 of row r: 16-byte chunks 4*half .. 4*half+3 of the
             // 128-byte row, stored with the 128-byte swizzle
             uint4 raw[4];
@@ -786,7 +899,10 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
               const uint32_t in[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
               for (int t = 0; t < 4; ++t) {
-                e4m3x4_to_bf16x4(in[t], w[8 * i + 2 * t], w[8 * i + 2 * t + 1]);
+                if (kind_f16(KIND))
+                  e4m3x4_to_f16x4(in[t], w[8 * i + 2 * t], w[8 * i + 2 * t + 1]);
+                else
+                  e4m3x4_to_bf16x4(in[t], w[8 * i + 2 * t], w[8 * i + 2 * t + 1]);
               }
             }
           } else {
@@ -808,6 +924,17 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
               mbar_arrive(&s_empty[slot]);
             }
             ++is;
+            if (KIND == KIND_MXH) {
+              const int emax = static_cast<int>(max_byte(e4));
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int e = static_cast<int>((e4 >> (8 * (2 * half + k))) & 0xFFu);
+                const uint32_t f2 = f16_pow2(e - emax) * 0x10001u;
+                const uint32_t in[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) e2m1x8_to_f16x8(in[j], f2, &w[16 * k + 4 * j]);
+              }
+            } else
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               const uint32_t e = (e4 >> (8 * (2 * half + k))) & 0xFFu;
@@ -1192,9 +1319,16 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
                 const float4 v = *reinterpret_cast<const float4*>(&stg[jj * 128 + nl]);
                 const float vv[4] = {v.x, v.y, v.z, v.w};
                 float* dst = reinterpret_cast<float*>(p.out) + static_cast<int64_t>(slot) * p.ldo;
+                const bool v4 = p.vec_ok && n + 3 < p.N;
+                if (v4) {
+                  *reinterpret_cast<float4*>(dst + n) =
+                      make_float4((vv[0] + b4[0]) * rw, (vv[1] + b4[1]) * rw, (vv[2] + b4[2]) * rw,
+                                  (vv[3] + b4[3]) * rw);
+                } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  if (n + i < p.N) dst[n + i] = (vv[i] + b4[i]) * rw;
+                  for (int i = 0; i < 4; ++i)
+                    if (n + i < p.N) dst[n + i] = (vv[i] + b4[i]) * rw;
+                }
                 if (p.combine_cnt != nullptr) {
                   // the last of the token's topk slots to reach this tile
                   // sums them (release: fence before the count; acquire: fence
@@ -1214,9 +1348,17 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
                     for (int k = 0; k < p.topk; ++k) {
                       const float* yr = reinterpret_cast<const float*>(p.out) +
                                         (static_cast<int64_t>(t) * p.topk + k) * p.ldo;
+                      if (v4) {
+                        const float4 y4 = __ldcg(reinterpret_cast<const float4*>(yr + n));
+                        s4[0] += y4.x;
+                        s4[1] += y4.y;
+                        s4[2] += y4.z;
+                        s4[3] += y4.w;
+                      } else {
 #pragma unroll
-                      for (int i = 0; i < 4; ++i)
-                        if (n + i < p.N) s4[i] += __ldcg(yr + n + i);
+                        for (int i = 0; i < 4; ++i)
+                          if (n + i < p.N) s4[i] += __ldcg(yr + n + i);
+                      }
                     }
                     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.combine_out) +
                                        static_cast<int64_t>(t) * p.combine_ldo;

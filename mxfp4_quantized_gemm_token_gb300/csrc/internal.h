@@ -89,7 +89,12 @@ cudaError_t launch_moe_align(const int32_t* topk_ids, int64_t S, int32_t E, int3
 cudaError_t launch_gather_rows(const void* hidden, int64_t ldh, int64_t K, int32_t topk,
                                const int32_t* sorted_ids, const int32_t* offsets,
                                const int32_t* num_blocks, int32_t block_m, int64_t cap, void* xs,
-                               int* zero, int64_t nzero, cudaStream_t stream);
+                               int* zero, int64_t nzero, const float* tscale, float* rscale,
+                               cudaStream_t stream);
+
+cudaError_t launch_rows_to_f16(const void* src, int64_t rows, int64_t K, int64_t ld,
+                               const int32_t* count, void* dst, float* rscale,
+                               cudaStream_t stream);
 
 cudaError_t launch_combine(const float* y, int64_t T, int32_t topk, int64_t K, void* out,
                            int64_t ldo, cudaStream_t stream);

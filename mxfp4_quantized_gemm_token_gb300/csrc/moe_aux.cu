@@ -2,6 +2,7 @@
 // alignment, the token-row gather that feeds stage 1, the top-k combine, and
 // the small helpers (split-K reduction of fp8_scaled_mm, debug unsort).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "internal.h"
 
@@ -173,6 +174,78 @@ cudaError_t launch_moe_align(const int32_t* topk_ids, int64_t S, int32_t E, int3
                   expert_ids, offsets, num_blocks, status);
 }
 
+// --------------------------------------------------------- rows to f16
+// The f16 MMA operand of the fused MoE: each bf16 row x (K values) becomes
+// x * 2^p in f16 with p = 14 - floor(log2(max |x|)) (the row maximum lands in
+// [2^14, 2^15), below the f16 maximum), and rscale = 2^-p undoes it in the
+// epilogue.  Power-of-two scaling is exact, and so is the f16 value of every
+// element not more than ~2^31 below its row maximum (bf16's 8 significant
+// bits then stay inside f16's range); an all-zero row keeps p = 0.  One warp
+// per row; `rows` may be read on the device (count != NULL).
+__global__ void rows_to_f16_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows, int64_t K,
+                                   int64_t ld, const int32_t* __restrict__ count,
+                                   __half* __restrict__ dst, float* __restrict__ rscale, int vec) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t nrows = count != nullptr ? static_cast<int64_t>(__ldg(count)) : rows;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < nrows;
+       r += nwarps) {
+    const __nv_bfloat16* s = src + r * ld;
+    float m = 0.f;
+    if (vec) {
+      for (int64_t k = lane * 8; k < K; k += 256) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(s + k));
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          m = fmaxf(m, fabsf(__uint_as_float(wv[i] << 16)));
+          m = fmaxf(m, fabsf(__uint_as_float(wv[i] & 0xFFFF0000u)));
+        }
+      }
+    } else {
+      for (int64_t k = lane; k < K; k += 32) m = fmaxf(m, fabsf(__bfloat162float(s[k])));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    int pw = 0;
+    if (m > 0.f) pw = max(-126, min(126, 14 - ilogbf(m)));
+    const float up = ldexpf(1.0f, pw);
+    if (lane == 0) rscale[r] = ldexpf(1.0f, -pw);
+    __half* d = dst + r * K;
+    if (vec) {
+      for (int64_t k = lane * 8; k < K; k += 256) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(s + k));
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          __half2 h = __floats2half2_rn(__uint_as_float(wv[i] << 16) * up,
+                                        __uint_as_float(wv[i] & 0xFFFF0000u) * up);
+          o[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(d + k) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    } else {
+      for (int64_t k = lane; k < K; k += 32) d[k] = __float2half_rn(__bfloat162float(s[k]) * up);
+    }
+  }
+}
+
+cudaError_t launch_rows_to_f16(const void* src, int64_t rows, int64_t K, int64_t ld,
+                               const int32_t* count, void* dst, float* rscale,
+                               cudaStream_t stream) {
+  const int vec = (K % 8 == 0) && (ld % 8 == 0) && (reinterpret_cast<uintptr_t>(src) & 15) == 0 &&
+                  (reinterpret_cast<uintptr_t>(dst) & 15) == 0;
+  int64_t blocks = (rows + 7) / 8;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  return launch_k(rows_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                  reinterpret_cast<const __nv_bfloat16*>(src), rows, K, ld, count,
+                  reinterpret_cast<__half*>(dst), rscale, vec);
+}
+
 // ------------------------------------------------------------ row gather
 // Stage-1 operand: compact row r = offsets[b] + m holds hidden[slot / topk],
 // slot = sorted_ids[b*block_m + m] (the page copies the same rows per block
@@ -182,7 +255,8 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int
                                    const int32_t* __restrict__ offsets,
                                    const int32_t* __restrict__ num_blocks, int BM,
                                    __nv_bfloat16* __restrict__ xs, int vec, int* __restrict__ zero,
-                                   int64_t nzero) {
+                                   int64_t nzero, const float* __restrict__ tscale,
+                                   float* __restrict__ rscale) {
   pdl_wait();
   pdl_launch_dependents();
   // also clears the fused combine's counters for this call
@@ -201,6 +275,7 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int
     const int slot = __ldg(sorted_ids + w);
     const __nv_bfloat16* src = hidden + static_cast<int64_t>(slot / topk) * ldh;
     __nv_bfloat16* dst = xs + static_cast<int64_t>(r0 + m) * K;
+    if (rscale != nullptr && lane == 0) rscale[r0 + m] = __ldg(tscale + slot / topk);
     if (vec) {
       for (int64_t k = lane * 8; k < K; k += 256)
         *reinterpret_cast<uint4*>(dst + k) = __ldg(reinterpret_cast<const uint4*>(src + k));
@@ -213,7 +288,8 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int
 cudaError_t launch_gather_rows(const void* hidden, int64_t ldh, int64_t K, int32_t topk,
                                const int32_t* sorted_ids, const int32_t* offsets,
                                const int32_t* num_blocks, int32_t block_m, int64_t cap, void* xs,
-                               int* zero, int64_t nzero, cudaStream_t stream) {
+                               int* zero, int64_t nzero, const float* tscale, float* rscale,
+                               cudaStream_t stream) {
   const int vec = (K % 8 == 0) && (ldh % 8 == 0) &&
                   (reinterpret_cast<uintptr_t>(hidden) & 15) == 0 &&
                   (reinterpret_cast<uintptr_t>(xs) & 15) == 0;
@@ -224,7 +300,7 @@ cudaError_t launch_gather_rows(const void* hidden, int64_t ldh, int64_t K, int32
   return launch_k(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
                   reinterpret_cast<const __nv_bfloat16*>(hidden), ldh, K, topk, sorted_ids,
                   offsets, num_blocks, block_m, reinterpret_cast<__nv_bfloat16*>(xs), vec, zero,
-                  zero != nullptr ? nzero : 0);
+                  zero != nullptr ? nzero : 0, tscale, rscale);
 }
 
 // ------------------------------------------------------------ combine

@@ -216,5 +216,21 @@ def test_fused_combine_is_bit_identical_to_the_combine_kernel(oracle, wtype, T, 
             outs.append(run_moe(oracle, wtype, E, N, K, x, tw, ids, 16, bias=(wtype == W_MX),
                                 check_ckpt=False))
     finally:
-        mxq.set_option(_lib.OPT_FUSE_COMBINE, 1)
+        mxq.set_option(_lib.OPT_FUSE_COMBINE, 0)
     assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("mode", [0, 2])
+@pytest.mark.parametrize("wtype,block_m", [(W_FP8, 32), (W_MX, 32), (W_FP8, 64), (W_MX, 64)])
+def test_fused_operand_modes(oracle, mode, wtype, block_m):
+    """The expert GEMMs with bf16 operands (mode 0) and with f16 operands for
+    both weight formats (mode 2), against the oracle with the checkpoints and
+    the stage-accumulator probes (the default mode 1 runs everywhere else)."""
+    E, N, K, T, topk = 12, 256, 384, 40, 4
+    x = synth.activations(T, K, seed=91, scale_div=10)
+    tw, ids = synth.routing_zipf(T, E, topk, seed=92)
+    try:
+        mxq.set_option(_lib.OPT_MOE_F16, mode)
+        run_moe(oracle, wtype, E, N, K, x, tw, ids, block_m, bias=(wtype == W_MX))
+    finally:
+        mxq.set_option(_lib.OPT_MOE_F16, 1)
