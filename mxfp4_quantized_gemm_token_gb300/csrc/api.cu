@@ -655,7 +655,8 @@ extern "C" mxq_status mxq_moe_align_block(const int32_t* topk_ids, int64_t T, in
 namespace {
 
 struct MoeWs {
-  size_t sorted, experts, offsets, nblocks, xs, ic1, y, cnt, hf16, tscale, rs1, ic1h, rs2, total;
+  size_t sorted, experts, offsets, nblocks, xs, ic1, y, cnt, hf16, tscale, rs1, ic1h, rs2, emax,
+      total;
   int64_t S, cap, ncnt;
 };
 
@@ -704,6 +705,9 @@ MoeWs moe_ws(int64_t T, int64_t K, int32_t E, int64_t N, int32_t topk, int32_t b
   o = round_up(o + static_cast<size_t>(w.S) * N * 2, 256);
   w.rs2 = o;
   o = round_up(o + static_cast<size_t>(w.S) * 4, 256);
+  // MXFP4 with f16 operands: the largest scale exponent of every expert row
+  w.emax = o;
+  o = round_up(o + static_cast<size_t>(E) * std::max<int64_t>(2 * N, K), 256);
   w.total = o;
   return w;
 }
@@ -768,6 +772,7 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
   float* rs1 = reinterpret_cast<float*>(ws + w.rs1);
   void* ic1h = ws + w.ic1h;
   float* rs2 = reinterpret_cast<float*>(ws + w.rs2);
+  uint8_t* emax = ws + w.emax;
 
   cudaError_t e = launch_moe_align(topk_ids, w.S, E, block_m, sorted_ids, expert_ids, offsets,
                                    nblocks, w.cap, d.status, st);
@@ -875,6 +880,11 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
       p.sa0 = 1;
       p.sa1 = 0;
     }
+    if (kind == KIND_MXH) {
+      e = launch_mx_row_emax(wsc, rows, red / 32, red / 32, expert_ids, nblocks, E, w.cap, emax, st);
+      if (e != cudaSuccess) return cuda_fail(e, "MXFP4 row exponent launch");
+      p.mx_emax = emax;
+    }
     p.bias = stage == 0 ? w1_bias : w2_bias;
     p.bias_dtype = MXQ_F32;
     p.bias_e = rows;
@@ -896,7 +906,7 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
     p.inject_stall = static_cast<int>(option(MXQ_OPT_INJECT_STALL));
     const int64_t units = w.cap * p.tiles_n;
     const int grid = static_cast<int>(std::min<int64_t>(units, sms));
-    e = launch_gemm(kind, stage == 0 ? EPI_SILU : EPI_SCATTER, bt, fp8 || f16, maps, p, grid, st);
+    e = launch_gemm(kind, stage == 0 ? EPI_SILU : EPI_SCATTER, bt, fp8, maps, p, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, stage == 0 ? "stage-1 launch" : "stage-2 launch");
   }
   if (!fuse_combine) {

@@ -56,8 +56,9 @@ namespace mxq {
 // KIND_F8H / KIND_MXH (the fused MoE): the same weights decoded to f16, one
 // conversion instruction per pair; the tokens are f16 rows pre-scaled by a
 // power of two whose inverse is the column scale.  MXH decodes each 32-group
-// as e2m1 * 2^(e - emax) with emax the largest ue8m0 exponent of the row's
-// 128-wide slice; 2^(emax - 127) is the row's promotion factor of the slice.
+// as e2m1 * 2^(e - emax) with emax the largest ue8m0 exponent of the whole
+// weight row (mx_emax), accumulates over all of K, and the epilogue applies
+// 2^(emax - 127) per row and the token scale per column once.
 enum { KIND_F8F8 = 0, KIND_F8W = 1, KIND_MXW = 2, KIND_F8H = 3, KIND_MXH = 4 };
 __host__ __device__ constexpr bool kind_mx(int k) { return k == KIND_MXW || k == KIND_MXH; }
 __host__ __device__ constexpr bool kind_f8w(int k) { return k == KIND_F8W || k == KIND_F8H; }
@@ -107,6 +108,7 @@ struct GemmParams {
   int64_t sw0, sw1, sw_e;
   int block_n;        // 0 = per-tensor (w_scale[0]); 1 or 128 = block rows
   const uint8_t* mx_scale;
+  const uint8_t* mx_emax;   // MXH: largest ue8m0 exponent of each weight row [rows_total]
   int64_t mx_ld;
   int mx_cols;
   int64_t mx_rows_total;
@@ -198,7 +200,6 @@ struct Layout {
   static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory over budget");
   static_assert(COLS % 32 == 0 && COLS <= 128, "epilogue column split");
   static_assert(SSLOTS * BT * 4 <= 8192, "scale ring size");
-  static_assert(KIND != KIND_MXH || SSLOTS * BT * 4 <= 4096, "f16 MXFP4 column scales and bytes overlap");
 };
 
 struct Unit {
@@ -361,11 +362,6 @@ __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t word, uint32_t f2, uint
 __device__ __forceinline__ uint32_t f16_pow2(int d) {
   return d >= -14 ? static_cast<uint32_t>(d + 15) << 10 : (d >= -24 ? 1u << (d + 24) : 0u);
 }
-// largest byte of a 32-bit word
-__device__ __forceinline__ uint32_t max_byte(uint32_t w) {
-  const uint32_t m = __vmaxu4(w, w >> 16);
-  return __vmaxu4(m, m >> 8) & 0xFFu;
-}
 
 // Barrier of the 128 epilogue threads on an mbarrier, so that it is bounded
 // like every other wait (a plain bar.sync would hang if one warp gave up).
@@ -412,13 +408,13 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   // MXFP4: [SSL][128] ue8m0 bytes of one slice, 4 per weight row (shares
   // sAsc for bf16 decode; its own area for f16 decode, whose slots also
   // carry column scales, BT <= 128)
-  uint32_t* sMx = reinterpret_cast<uint32_t*>(misc + 1024 + (KIND == KIND_MXH ? 4096 : 0));
+  uint32_t* sMx = reinterpret_cast<uint32_t*>(misc + 1024);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   WaitCtx wc{p.status, abort_flag, p.budget_ns};
   // a row scale per TMEM lane is needed when Ws is not uniform over the tile
-  const bool lane_ws = PROMOTE && (p.block_n == 1 || EPI == EPI_SILU || KIND == KIND_MXH);
+  const bool lane_ws = PROMOTE && (p.block_n == 1 || EPI == EPI_SILU);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < AS; ++i) {
@@ -441,7 +437,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       mbar_init(&s_full[i], 1);
       // MXFP4 slots feed one decode group (bf16) or a decode group and the
       // epilogue (f16, per-slice promotion)
-      mbar_init(&s_empty[i], KIND == KIND_MXW ? 8 : (KIND == KIND_MXH ? 8 + 4 * EW : 4 * EW));
+      mbar_init(&s_empty[i], kind_mx(KIND) ? 8 : 4 * EW);
     }
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
@@ -669,7 +665,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     // ------------------------------------------------------ scale loader
     if (KIND == KIND_F8W && !PROMOTE) {
       // per-tensor weights: no slice scales
-    } else if (KIND == KIND_MXW) {
+    } else if (kind_mx(KIND)) {
       // ue8m0 bytes of each slice (4 groups of 32 along K per weight row),
       // MLA slices ahead in registers; rows of a ragged tail clamp to the
       // last row and columns past K read 127 (2^0; the data there is zero).
@@ -728,72 +724,6 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         }
       }
     mx_done:;
-    } else if (KIND == KIND_MXH) {
-      // MXFP4 decoded to f16, promoted per slice: each slot carries the
-      // slice's ue8m0 bytes (4 per weight row; past K: 0, the data there is
-      // zero), the row's factor 2^(emax - 127) and the column (token) scales
-      constexpr int MLA = 4;
-      constexpr int NA = BT / 32;
-      uint32_t is = 0;
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const Unit U = get_unit<EPI, BT>(p, u);
-        float ta[NA];
-#pragma unroll
-        for (int i = 0; i < NA; ++i) {
-          const int j = lane + 32 * i;
-          ta[i] = (p.a_scale != nullptr && j < U.rows) ? __ldg(p.a_scale + U.m0 + j) : 1.f;
-        }
-        uint32_t rb[MLA][4];
-        auto fetch = [&](int kb, uint32_t* b) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = lane + 32 * i;
-            int64_t grow = (EPI == EPI_SILU) ? static_cast<int64_t>(r < 64 ? U.wrow0 + r : U.wrow1 + (r - 64))
-                                             : static_cast<int64_t>(U.wrow0) + r;
-            if (grow >= p.mx_rows_total) grow = p.mx_rows_total - 1;
-            const uint8_t* rowp = p.mx_scale + grow * p.mx_ld + kb * 4;
-            if (p.mx_align >= 4 && kb * 4 + 4 <= p.mx_cols) {
-              b[i] = __ldg(reinterpret_cast<const uint32_t*>(rowp));
-            } else if (p.mx_align >= 2 && kb * 4 + 4 <= p.mx_cols) {
-              const uint16_t* hp = reinterpret_cast<const uint16_t*>(rowp);
-              b[i] = static_cast<uint32_t>(__ldg(hp)) | (static_cast<uint32_t>(__ldg(hp + 1)) << 16);
-            } else {
-              uint32_t v = 0;
-#pragma unroll
-              for (int c = 0; c < 4; ++c)
-                if (kb * 4 + c < p.mx_cols) v |= static_cast<uint32_t>(__ldg(rowp + c)) << (8 * c);
-              b[i] = v;
-            }
-          }
-        };
-#pragma unroll
-        for (int q = 0; q < MLA; ++q)
-          if (U.kb0 + q < U.kb1) fetch(U.kb0 + q, rb[q]);
-        for (int kb = U.kb0; kb < U.kb1; kb += MLA) {
-#pragma unroll
-          for (int q = 0; q < MLA; ++q) {
-            if (kb + q < U.kb1) {
-              const int slot = is % SSL;
-              if (!mbar_wait(&s_empty[slot], ((is / SSL) & 1) ^ 1, wc)) goto mxh_done;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int r = lane + 32 * i;
-                sMx[slot * 128 + r] = rb[q][i];
-                const uint32_t emax = max_byte(rb[q][i]);
-                // 2^(emax - 127) in fp32 (2^-127 is the subnormal 0x00400000)
-                sWr[slot * 128 + r] = __uint_as_float(emax != 0 ? emax << 23 : 0x00400000u);
-              }
-#pragma unroll
-              for (int i = 0; i < NA; ++i) sAsc[slot * BT + lane + 32 * i] = ta[i];
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&s_full[slot]);
-              ++is;
-              if (kb + q + MLA < U.kb1) fetch(kb + q + MLA, rb[q]);
-            }
-          }
-        }
-      }
-    mxh_done:;
     } else if (EPI == EPI_NORMAL) {
       // token-major: the epilogue threads read their own slice scales
     } else if (PROMOTE) {
@@ -872,6 +802,13 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       uint32_t ia = 0, ic = 0, is = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
+        int emax = 0;   // MXH: the row's largest scale exponent (the f16 reference)
+        if (KIND == KIND_MXH) {
+          int64_t grow = (EPI == EPI_SILU) ? static_cast<int64_t>(r < 64 ? U.wrow0 + r : U.wrow1 + (r - 64))
+                                           : static_cast<int64_t>(U.wrow0) + r;
+          if (grow >= p.mx_rows_total) grow = p.mx_rows_total - 1;
+          emax = __ldg(p.mx_emax + grow);
+        }
         for (int kb = U.kb0; kb < U.kb1; ++kb, ++ia, ++ic) {
           if (L::NDG > 1 && ia % L::NDG != grp) {
             if (kind_mx(KIND)) ++is;   // the other group's scale slot
@@ -925,7 +862,6 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
             }
             ++is;
             if (KIND == KIND_MXH) {
-              const int emax = static_cast<int>(max_byte(e4));
 #pragma unroll
               for (int k = 0; k < 2; ++k) {
                 const int e = static_cast<int>((e4 >> (8 * (2 * half + k))) & 0xFFu);
@@ -1121,6 +1057,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       const int ngr = (colv + GRP - 1) / GRP;              // column groups with valid tokens
       float acc[COLS];
       float fscale = 1.f;
+      float rowf = 1.f;   // MXH: the weight row's 2^(emax - 127)
       uint32_t buf0 = 0, buf1 = 0;   // whole-K kinds: the unit's accumulator pair
       uint32_t rd0 = 0;              // the pair's first buffer to read
       bool two = false;
@@ -1184,6 +1121,13 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         }
       } else {
         if (p.block_n == 0 && p.w_scale != nullptr) fscale = __ldg(p.w_scale + U.e * p.sw_e);
+        if (KIND == KIND_MXH) {
+          int64_t grow = (EPI == EPI_SILU) ? static_cast<int64_t>(et < 64 ? U.wrow0 + et : U.wrow1 + (et - 64))
+                                           : static_cast<int64_t>(U.wrow0) + et;
+          if (grow >= p.mx_rows_total) grow = p.mx_rows_total - 1;
+          const uint32_t em = __ldg(p.mx_emax + grow);
+          rowf = __uint_as_float(em != 0 ? em << 23 : 0x00400000u);   // 2^(em - 127)
+        }
         // the unit's two accumulators (one per MMA issuer); the second is
         // unwritten when the unit has a single K slice
         const uint32_t tb0 = 2 * au, tb1 = 2 * au + 1;
@@ -1234,8 +1178,19 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < STG; ++j) v0[j] += v1[j];
               }
+              if (KIND == KIND_MXH) {
+                // row factor 2^(emax - 127), column factor = the token row's
+                // inverse pre-scale
 #pragma unroll
-              for (int j = 0; j < STG; ++j) stg[j * 128 + et] = v0[j] * fscale;
+                for (int j = 0; j < STG; ++j) {
+                  const int col = col0 + c * STG + j;
+                  const float cs = col < U.rows ? __ldg(p.a_scale + U.m0 + col) : 0.f;
+                  stg[j * 128 + et] = v0[j] * (rowf * cs);
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < STG; ++j) stg[j * 128 + et] = v0[j] * fscale;
+              }
             }
             if (!group_sync(&epi_bar[g], eph, wc)) goto epi_done;
             if (EPI == EPI_DENSE) {

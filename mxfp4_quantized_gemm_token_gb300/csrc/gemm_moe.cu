@@ -17,10 +17,10 @@ cudaError_t launch_gemm_moe(int kind, int epi, int bt, bool promote, const GemmM
     if (epi == EPI_SCATTER)
       return launch_gemm_bt<KIND_F8H, EPI_SCATTER, true>(bt, maps, p, grid, stream);
   } else if (kind == KIND_MXH) {
-    // MXFP4 decoded to f16: promoted per slice with the row's largest scale
-    if (epi == EPI_SILU) return launch_gemm_bt<KIND_MXH, EPI_SILU, true>(bt, maps, p, grid, stream);
+    // MXFP4 decoded to f16 relative to each row's largest scale: whole-K
+    if (epi == EPI_SILU) return launch_gemm_bt<KIND_MXH, EPI_SILU, false>(bt, maps, p, grid, stream);
     if (epi == EPI_SCATTER)
-      return launch_gemm_bt<KIND_MXH, EPI_SCATTER, true>(bt, maps, p, grid, stream);
+      return launch_gemm_bt<KIND_MXH, EPI_SCATTER, false>(bt, maps, p, grid, stream);
   } else if (kind == KIND_MXW) {
     // MXFP4: the ue8m0 scale is folded into the exact bf16 decode
     if (epi == EPI_SILU) return launch_gemm_bt<KIND_MXW, EPI_SILU, false>(bt, maps, p, grid, stream);

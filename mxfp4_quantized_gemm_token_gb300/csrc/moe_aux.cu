@@ -246,6 +246,46 @@ cudaError_t launch_rows_to_f16(const void* src, int64_t rows, int64_t K, int64_t
                   reinterpret_cast<__half*>(dst), rscale, vec);
 }
 
+// ------------------------------------------------ MXFP4 row exponents
+// The f16 decode of MXFP4 expert weights scales every 32-group relative to
+// the largest ue8m0 exponent of its weight row: emax[e * rows + r] = max over
+// k of scales[(e * rows + r) * ld + k].  Only the experts of the block table
+// are visited (a block whose expert repeats the previous block's is
+// skipped); one warp per row.
+__global__ void mx_row_emax_kernel(const uint8_t* __restrict__ scales, int64_t rows, int ncols,
+                                   int64_t ld, const int32_t* __restrict__ expert_ids,
+                                   const int32_t* __restrict__ num_blocks, int E,
+                                   uint8_t* __restrict__ emax) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int nb = __ldg(num_blocks);
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       w < static_cast<int64_t>(nb) * rows; w += nwarps) {
+    const int b = static_cast<int>(w / rows);
+    const int64_t r = w - static_cast<int64_t>(b) * rows;
+    const int e = __ldg(expert_ids + b);
+    if (e < 0 || e >= E || (b > 0 && __ldg(expert_ids + b - 1) == e)) continue;
+    const uint8_t* row = scales + (static_cast<int64_t>(e) * rows + r) * ld;
+    unsigned m = 0;
+    for (int k = lane; k < ncols; k += 32) m = max(m, static_cast<unsigned>(__ldg(row + k)));
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (lane == 0) emax[static_cast<int64_t>(e) * rows + r] = static_cast<uint8_t>(m);
+  }
+}
+
+cudaError_t launch_mx_row_emax(const void* scales, int64_t rows, int64_t ncols, int64_t ld,
+                               const int32_t* expert_ids, const int32_t* num_blocks, int E,
+                               int64_t cap, void* emax, cudaStream_t stream) {
+  int64_t blocks = (cap * rows + 7) / 8;
+  if (blocks > 8192) blocks = 8192;
+  if (blocks < 1) blocks = 1;
+  return launch_k(mx_row_emax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                  reinterpret_cast<const uint8_t*>(scales), rows, static_cast<int>(ncols), ld,
+                  expert_ids, num_blocks, E, reinterpret_cast<uint8_t*>(emax));
+}
+
 // ------------------------------------------------------------ row gather
 // Stage-1 operand: compact row r = offsets[b] + m holds hidden[slot / topk],
 // slot = sorted_ids[b*block_m + m] (the page copies the same rows per block
