@@ -100,18 +100,23 @@ enum {
                                GEMM (the last of a token's slots to finish a weight tile sums
                                its rows, ascending k); 0 (default, measured faster on GB300):
                                a separate combine kernel.  Bit-identical results either way. */
-  MXQ_OPT_MOE_F16 = 11      /* fused MoE operand type: 1 (default) f16 for FP8-block experts,
+  MXQ_OPT_MOE_F16 = 11,     /* fused MoE operand type: 1 (default) f16 for FP8-block experts,
                                bf16 for MXFP4; 2 f16 for both; 0 bf16 for both.  With f16 the
                                expert GEMMs multiply f16 operands:
                                weights decode to f16 in one conversion per pair (MXFP4
-                               groups scaled by 2^(e - emax of their 128-wide slice), the
-                               slice's 2^(emax-127) applied per row in fp32), and token
+                               groups scaled by 2^(e - emax of their weight row), the row's
+                               2^(emax-127) applied in fp32 by the epilogue), and token
                                rows are converted to f16 after a power-of-two row scaling
                                that the epilogue undoes; 0: bf16 operands (weights decoded
                                to bf16, tokens as given).  The f16 operands are exact
                                except for elements more than ~2^31 below their token row's
                                maximum and MXFP4 groups more than 2^23 below the largest
-                               group scale of their slice. */
+                               group scale of their row. */
+  MXQ_OPT_FUSE_QUANT = 12   /* mxq_w8a8_block_fp8_linear: 1 up to 32 token rows the activation
+                               quantization runs inside the GEMM; 0 (default, measured faster
+                               on GB300: the in-kernel IEEE divisions of four quantizer warps
+                               are latency-bound) a separate quantization kernel first.
+                               Bit-identical results. */
 };
 
 const char* mxq_last_error(void);
@@ -261,6 +266,30 @@ mxq_status mxq_fp8_scaled_mm_prepacked(const void* A, int32_t a_dtype, int64_t M
                                        int32_t bias_dtype, void* out, int32_t out_dtype,
                                        int64_t ldo, void* workspace, size_t ws_bytes,
                                        mxq_stream_t stream);
+
+/*
+ * Block-FP8 linear on bf16 activations ([XPU-FP8], torch_w8a8_block_fp8_linear
+ * excerpt: with no input scale the input is quantized per 1 x block_k group by
+ * per_token_group_quant_fp8 before scaled_mm):
+ *   out = fp8_scaled_mm(per_token_group_quant_fp8(x, 128, 1e-10), W, w_scale)
+ * x bf16 [M, K] (row stride ldx, 16-byte rows); W, w_scale, block_n in {1, 128},
+ * block_k = 128, bias, out as in mxq_fp8_scaled_mm.  With MXQ_OPT_FUSE_QUANT = 1,
+ * up to 32 rows the quantization runs inside the GEMM: each K slice of
+ * a token row is one 1 x 128 group, turned into e4m3 codes and a scale by the
+ * same IEEE arithmetic as mxq_per_token_group_quant_fp8, so codes, scales and
+ * output are bit-identical to the two-step path; otherwise the two steps run.
+ * workspace: mxq_w8a8_block_fp8_linear_workspace_size bytes (256-byte
+ * aligned; may be 0: then NULL), holding the quantized activations when not
+ * fused and the split-K partials.
+ */
+mxq_status mxq_w8a8_block_fp8_linear(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                     const void* W, int64_t N, int64_t ldw, const float* w_scale,
+                                     int32_t block_n, int32_t block_k, int64_t sw0, int64_t sw1,
+                                     const void* bias, int32_t bias_dtype, void* out,
+                                     int32_t out_dtype, int64_t ldo, void* workspace,
+                                     size_t ws_bytes, mxq_stream_t stream);
+mxq_status mxq_w8a8_block_fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K,
+                                                    int32_t block_n, size_t* bytes);
 
 /*
  * Batched scaled FP8 GEMM: `batch` independent mxq_fp8_scaled_mm problems of

@@ -307,6 +307,8 @@ def w8a8_block_fp8_linear(input, weight, block_size, weight_scale, input_scale=N
     if bk != 128 or bn not in (1, 128):
         raise ValueError("supported weight block sizes are [1, 128] and [128, 128], got %r"
                          % (list(block_size),))
+    if input_scale is None and input.dtype == torch.bfloat16 and not isinstance(weight, PackedWeight):
+        return _linear_bf16(input, weight, bn, weight_scale, bias)
     if input_scale is None:
         q, s = per_token_group_quant_fp8(input, bk)
         out_dtype = input.dtype
@@ -315,6 +317,36 @@ def w8a8_block_fp8_linear(input, weight, block_size, weight_scale, input_scale=N
         out_dtype = torch.bfloat16
     return fp8_scaled_mm(q, weight, weight_scale, [bn, bk], a_scale=s, bias=bias,
                          out_dtype=out_dtype)
+
+
+def _linear_bf16(x, w, bn, w_scale, bias):
+    """mxq_w8a8_block_fp8_linear: quantization per 1 x 128 group and the W8A8
+    GEMM in one call (fused into the GEMM for decode-size inputs)."""
+    _need_cuda(x, w, w_scale, bias)
+    lib = _lib_handle()
+    K = x.shape[-1]
+    x2 = _as_rows(x)
+    M = x2.shape[0]
+    if w.stride(-1) != 1:
+        w = w.contiguous()
+    N = w.shape[0]
+    if w_scale.dim() != 2:
+        raise ValueError("block weight scales must be 2-D")
+    bias_dtype = 0
+    if bias is not None:
+        if bias.dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError("bias must be fp32 or bf16")
+        bias_dtype = _lib.BF16 if bias.dtype == torch.bfloat16 else _lib.F32
+        bias = bias.contiguous()
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    sz = ctypes.c_size_t(0)
+    check(lib.mxq_w8a8_block_fp8_linear_workspace_size(M, N, K, bn, ctypes.byref(sz)))
+    ws = torch.empty(sz.value, dtype=torch.uint8, device=x.device) if sz.value else None
+    check(lib.mxq_w8a8_block_fp8_linear(
+        _ptr(x2), M, K, x2.stride(0), _ptr(w), N, w.stride(0), _ptr(w_scale), bn, 128,
+        w_scale.stride(0), w_scale.stride(1), _ptr(bias), bias_dtype, _ptr(out), _lib.BF16, N,
+        _ptr(ws), sz.value, _stream(x.device)))
+    return out.view(*x.shape[:-1], N)
 
 
 def fp8_per_tensor_linear(x, weight, scale, bias=None):

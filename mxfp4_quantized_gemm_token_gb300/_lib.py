@@ -21,8 +21,8 @@ BF16, F32, E4M3, E2M1X2, UE8M0 = 1, 2, 3, 4, 5
 W_FP8_BLOCK128, W_MXFP4 = 1, 2
 ACT_SILU, ACT_SWIGLU_CLAMP = 0, 1
 (OPT_SMALL_M_MAX, OPT_FORCE_PATH, OPT_WAIT_BUDGET_NS, OPT_SPLIT_K, OPT_INJECT_STALL, OPT_NUM_SMS,
- OPT_TILE_N, OPT_NORMAL_TILE, OPT_PDL, OPT_FUSE_COMBINE, OPT_MOE_F16) = (1, 2, 3, 4, 5, 6, 7, 8, 9, 10,
-                                                                   11)
+ OPT_TILE_N, OPT_NORMAL_TILE, OPT_PDL, OPT_FUSE_COMBINE, OPT_MOE_F16,
+ OPT_FUSE_QUANT) = (1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12)
 
 EXPORTED = [
     "mxq_last_error", "mxq_version", "mxq_set_option", "mxq_get_option", "mxq_sync_status",
@@ -31,6 +31,7 @@ EXPORTED = [
     "mxq_fused_experts_workspace_size", "mxq_fp8_scaled_mm_noalloc",
     "mxq_prepacked_weight_size", "mxq_prepack_weight", "mxq_fp8_scaled_mm_prepacked",
     "mxq_fp8_scaled_bmm", "mxq_quantize_mxfp4", "mxq_fused_experts_ex",
+    "mxq_w8a8_block_fp8_linear", "mxq_w8a8_block_fp8_linear_workspace_size",
 ]
 
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -68,6 +69,10 @@ def _declare(lib):
                                     I64, I64, P, I32, I32, I64, I64, I64, P, I32, I64, P, I32,
                                     I64, I64, P]),
         "mxq_quantize_mxfp4": (st, [P, I32, I64, I64, I64, P, P, P]),
+        "mxq_w8a8_block_fp8_linear": (st, [P, I64, I64, I64, P, I64, I64, P, I32, I32, I64,
+                                           I64, P, I32, P, I32, I64, P, SZ, P]),
+        "mxq_w8a8_block_fp8_linear_workspace_size": (st, [I64, I64, I64, I32,
+                                                          ctypes.POINTER(SZ)]),
         "mxq_moe_align_block": (st, [P, I64, I32, I32, I32, P, P, P, P, I64, P, SZ, P]),
         "mxq_fused_experts": (st, [P, I64, I64, I64, I32, I32, I64, P, P, P, P, P, P, P, P, I32,
                                    I32, P, I64, P, SZ, P]),

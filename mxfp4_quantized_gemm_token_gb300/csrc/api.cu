@@ -29,7 +29,7 @@ mxq_status cuda_fail(cudaError_t e, const char* what) {
   return fail(MXQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-std::atomic<int64_t> g_opts[12] = {0, 4, 0, 2000000000LL, 0, 0, 0, 0, 0, 1, 0, 1};
+std::atomic<int64_t> g_opts[13] = {0, 4, 0, 2000000000LL, 0, 0, 0, 0, 0, 1, 0, 1, 0};
 
 std::mutex g_dev_mu;
 DeviceInfo g_devs[64];
@@ -135,7 +135,7 @@ extern "C" const char* mxq_last_error(void) { return g_err.c_str(); }
 extern "C" const char* mxq_version(void) { return "mxq 0.1 (sm_103a, tcgen05)"; }
 
 extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
-  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_MOE_F16)
+  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_FUSE_QUANT)
     return fail(MXQ_ERR_INVALID_ARG, "unknown option " + std::to_string(opt));
   if (opt == MXQ_OPT_NORMAL_TILE && value != 0 && value != 128 && value != 192 && value != 256)
     return fail(MXQ_ERR_INVALID_ARG, "NORMAL_TILE is 0 (auto), 128, 192 or 256");
@@ -143,8 +143,9 @@ extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
       value != 256)
     return fail(MXQ_ERR_INVALID_ARG, "TILE_N is 0 (auto), 32, 64, 128 or 256");
   if (value < 0) return fail(MXQ_ERR_INVALID_ARG, "option values are non-negative");
-  if ((opt == MXQ_OPT_PDL || opt == MXQ_OPT_FUSE_COMBINE) && value != 0 && value != 1)
-    return fail(MXQ_ERR_INVALID_ARG, "PDL and FUSE_COMBINE are 0 (off) or 1 (on)");
+  if ((opt == MXQ_OPT_PDL || opt == MXQ_OPT_FUSE_COMBINE || opt == MXQ_OPT_FUSE_QUANT) &&
+      value != 0 && value != 1)
+    return fail(MXQ_ERR_INVALID_ARG, "PDL, FUSE_COMBINE and FUSE_QUANT are 0 (off) or 1 (on)");
   if (opt == MXQ_OPT_MOE_F16 && value > 2)
     return fail(MXQ_ERR_INVALID_ARG, "MOE_F16 is 0, 1 or 2");
   if (opt == MXQ_OPT_FORCE_PATH && value > 3)
@@ -155,7 +156,7 @@ extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
 }
 
 extern "C" mxq_status mxq_get_option(int32_t opt, int64_t* value) {
-  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_MOE_F16 || value == nullptr)
+  if (opt < MXQ_OPT_SMALL_M_MAX || opt > MXQ_OPT_FUSE_QUANT || value == nullptr)
     return fail(MXQ_ERR_INVALID_ARG, "unknown option or NULL value");
   *value = g_opts[opt].load();
   return MXQ_OK;
@@ -616,6 +617,151 @@ extern "C" mxq_status mxq_fp8_scaled_bmm(
   cudaError_t e = launch_gemm(pl.kind, EPI_DENSE, pl.bt, pl.promote, maps, p, grid,
                               reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "scaled-bmm launch");
+  return MXQ_OK;
+}
+
+// ------------------------------------------------ block-FP8 linear (bf16 in)
+
+namespace {
+
+// token rows up to which the linear quantizes inside the GEMM (one 32-wide
+// token tile; every weight tile re-quantizes the tokens it needs)
+constexpr int64_t kFusedQuantMaxM = 32;
+
+struct LinearWs {
+  size_t q, s, part, total;
+  bool fused;
+};
+
+mxq_status linear_ws(int64_t M, int64_t N, int64_t K, int32_t block_n, int sms, LinearWs* w) {
+  const MmPlan pl = plan_for_call(M, N, K, MXQ_E4M3, block_n, 128, sms);
+  w->fused = M <= kFusedQuantMaxM && option(MXQ_OPT_FUSE_QUANT) != 0 && !pl.normal && pl.bt == 32;
+  size_t o = 0;
+  w->q = w->s = 0;
+  if (!w->fused) {
+    w->q = o;
+    o = round_up(o + static_cast<size_t>(M) * K, 256);
+    w->s = o;
+    o = round_up(o + static_cast<size_t>(M) * cdiv(K, 128) * sizeof(float), 256);
+  }
+  w->part = o;
+  o = round_up(o + plan_workspace_bytes(pl, M, N), 256);
+  w->total = o;
+  return MXQ_OK;
+}
+
+}  // namespace
+
+extern "C" mxq_status mxq_w8a8_block_fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K,
+                                                               int32_t block_n, size_t* bytes) {
+  if (!bytes || M < 0 || N < 0 || K <= 0)
+    return fail(MXQ_ERR_INVALID_ARG, "bad sizes or NULL result pointer");
+  if (block_n != 1 && block_n != 128)
+    return fail(MXQ_ERR_UNSUPPORTED, "block_n must be 1 or 128");
+  *bytes = 0;
+  if (M == 0 || N == 0) return MXQ_OK;
+  DeviceInfo d;
+  std::string err;
+  if (!device_info(&d, &err)) return fail(MXQ_ERR_UNSUPPORTED, err);
+  LinearWs w;
+  linear_ws(M, N, K, block_n, sms_for_grid(d), &w);
+  *bytes = w.total;
+  return MXQ_OK;
+}
+
+extern "C" mxq_status mxq_w8a8_block_fp8_linear(
+    const void* x, int64_t M, int64_t K, int64_t ldx, const void* W, int64_t N, int64_t ldw,
+    const float* w_scale, int32_t block_n, int32_t block_k, int64_t sw0, int64_t sw1,
+    const void* bias, int32_t bias_dtype, void* out, int32_t out_dtype, int64_t ldo,
+    void* workspace, size_t ws_bytes, mxq_stream_t stream) {
+  if (M < 0 || N < 0 || K <= 0) return fail(MXQ_ERR_INVALID_ARG, "need M, N >= 0 and K > 0");
+  if (!(block_k == 128 && (block_n == 1 || block_n == 128)))
+    return fail(MXQ_ERR_UNSUPPORTED,
+                "weight block size must be [128, 128] or [1, 128]; got [" +
+                    std::to_string(block_n) + ", " + std::to_string(block_k) + "]");
+  if (M == 0 || N == 0) return MXQ_OK;
+  if (!x) return fail(MXQ_ERR_INVALID_ARG, "x must be non-NULL");
+  if (ldx < K) return fail(MXQ_ERR_INVALID_ARG, "ldx must be >= K");
+  if (!aligned16(x) || (ldx * 2) % 16 != 0)
+    return fail(MXQ_ERR_UNSUPPORTED, "x needs a 16-byte aligned base and rows a multiple of 16 bytes");
+  // the rest of the checks are those of the W8A8 GEMM (a stand-in pointer for
+  // the quantized activations and their scales)
+  const mxq_status vst =
+      validate_mm(x, MXQ_E4M3, M, K, cdiv(K, 16) * 16, w_scale, 1, 1, W, N, ldw, w_scale, block_n,
+                  block_k, sw0, sw1, bias, bias_dtype, out, out_dtype, ldo);
+  if (vst != MXQ_OK) return vst;
+  DeviceInfo d;
+  std::string err;
+  if (!device_info(&d, &err)) return fail(MXQ_ERR_UNSUPPORTED, err);
+  LinearWs w;
+  linear_ws(M, N, K, block_n, sms_for_grid(d), &w);
+  if (w.total > 0 && (workspace == nullptr || ws_bytes < w.total ||
+                      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0))
+    return fail(MXQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned and hold " +
+                                         std::to_string(w.total) +
+                                         " bytes (mxq_w8a8_block_fp8_linear_workspace_size)");
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!w.fused) {
+    // separate per-token-group quantization, then the W8A8 GEMM
+    if (K % 16 != 0)
+      return fail(MXQ_ERR_UNSUPPORTED,
+                  "above the fused-quantization size, K must be a multiple of 16");
+    void* q = ws + w.q;
+    float* sc = reinterpret_cast<float*>(ws + w.s);
+    cudaError_t e = launch_group_quant(x, M, K, ldx, 128, 1e-10f, q, sc, d.num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "group quant launch");
+    return scaled_mm_run(q, MXQ_E4M3, M, K, K, sc, cdiv(K, 128), 1, W, N, ldw, nullptr, w_scale,
+                         block_n, block_k, sw0, sw1, bias, bias_dtype, out, out_dtype, ldo,
+                         w.total > w.part ? ws + w.part : nullptr, w.total - w.part, stream);
+  }
+  // fused: bf16 tokens are quantized per 1 x 128 group inside the GEMM
+  const int sms = sms_for_grid(d);
+  MmPlan pl = plan_for_call(M, N, K, MXQ_E4M3, block_n, block_k, sms);
+  GemmMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  if (!make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, K, N, ldw, 128, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B, &err) ||
+      !make_map_2d(&maps.b[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, 64, 32,
+                   CU_TENSOR_MAP_SWIZZLE_128B, &err))
+    return fail(MXQ_ERR_CUDA, err);
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.nkb = pl.nkb;
+  p.tiles_n = pl.tiles_n;
+  p.tiles_m = pl.tiles_m;
+  p.splits = pl.splits;
+  p.kb_per_split = pl.kb_per_split;
+  p.a_scale = nullptr;   // the group scales come from the quantizer warps
+  p.w_scale = w_scale;
+  p.sw0 = sw0;
+  p.sw1 = sw1;
+  p.block_n = block_n;
+  p.bias = bias;
+  p.bias_dtype = bias ? bias_dtype : 0;
+  p.out = out;
+  p.out_dtype = out_dtype;
+  p.ldo = ldo;
+  p.partial = pl.splits > 1 ? reinterpret_cast<float*>(ws + w.part) : nullptr;
+  p.npad = static_cast<int>(cdiv(N, 128) * 128);
+  p.q_eps = 1e-10f;
+  p.status = d.status;
+  p.budget_ns = static_cast<unsigned long long>(option(MXQ_OPT_WAIT_BUDGET_NS));
+  p.inject_stall = static_cast<int>(option(MXQ_OPT_INJECT_STALL));
+  const uintptr_t ob = reinterpret_cast<uintptr_t>(out);
+  p.vec_ok = (ldo % 4 == 0) && ((out_dtype == MXQ_BF16) ? (ob & 7) == 0 : (ob & 15) == 0);
+  const int64_t units = static_cast<int64_t>(pl.tiles_n) * pl.tiles_m * pl.splits;
+  const int grid = static_cast<int>(std::min<int64_t>(units, sms));
+  cudaError_t e = launch_gemm(KIND_F8Q, EPI_DENSE, 32, true, maps, p, grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "fused linear launch");
+  if (pl.splits > 1) {
+    e = launch_splitk_reduce(p.partial, pl.splits, M, N, bias, p.bias_dtype, out, out_dtype, ldo,
+                             st);
+    if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
+  }
   return MXQ_OK;
 }
 

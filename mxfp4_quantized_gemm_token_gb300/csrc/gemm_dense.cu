@@ -20,6 +20,11 @@ cudaError_t launch_gemm(int kind, int epi, int bt, bool promote, const GemmMaps&
     return cudaErrorInvalidValue;
   }
   if (epi != EPI_DENSE) return launch_gemm_moe(kind, epi, bt, promote, maps, p, grid, stream);
+  if (kind == KIND_F8Q) {
+    // decode-size W8A8 with the activation quantization inside the GEMM
+    if (bt == 32) return launch_gemm_inst<KIND_F8Q, EPI_DENSE, 32, true>(maps, p, grid, stream);
+    return cudaErrorInvalidValue;
+  }
   if (kind == KIND_F8F8) {
     // activation group scales always present: every slice is promoted
     return launch_gemm_bt<KIND_F8F8, EPI_DENSE, true>(bt, maps, p, grid, stream);

@@ -59,7 +59,11 @@ namespace mxq {
 // as e2m1 * 2^(e - emax) with emax the largest ue8m0 exponent of the whole
 // weight row (mx_emax), accumulates over all of K, and the epilogue applies
 // 2^(emax - 127) per row and the token scale per column once.
-enum { KIND_F8F8 = 0, KIND_F8W = 1, KIND_MXW = 2, KIND_F8H = 3, KIND_MXH = 4 };
+// KIND_F8Q: FP8 weights x bf16 activations quantized inside the kernel per
+// 1 x 128 group (each group is one K slice of a token row) to e4m3, then the
+// FP8 x FP8 product of KIND_F8F8 (decode-size W8A8 with the quantization fused).
+enum { KIND_F8F8 = 0, KIND_F8W = 1, KIND_MXW = 2, KIND_F8H = 3, KIND_MXH = 4, KIND_F8Q = 5 };
+__host__ __device__ constexpr bool kind_f8mma(int k) { return k == KIND_F8F8 || k == KIND_F8Q; }
 __host__ __device__ constexpr bool kind_mx(int k) { return k == KIND_MXW || k == KIND_MXH; }
 __host__ __device__ constexpr bool kind_f8w(int k) { return k == KIND_F8W || k == KIND_F8H; }
 __host__ __device__ constexpr bool kind_f16(int k) { return k == KIND_F8H || k == KIND_MXH; }
@@ -135,6 +139,7 @@ struct GemmParams {
   // 128-byte-swizzled shared-memory image; rows up to npad exist
   const uint8_t* wpacked;
   int npad;
+  float q_eps;         // F8Q: the group-scale floor (s = max(amax, q_eps) / 448)
   int* status;
   unsigned long long budget_ns;
   int inject_stall;
@@ -145,7 +150,7 @@ template <int KIND, int BT, int EPI>
 struct Layout {
   // epilogue warpgroups: one for up to 64 columns, two for 128; FP8 x FP8
   // tiles of 192 / 256 columns use three / four (64 columns each)
-  static constexpr int EW = (KIND == KIND_F8F8 && BT >= 192) ? BT / 64 : (BT >= 128 ? 2 : 1);
+  static constexpr int EW = (kind_f8mma(KIND) && BT >= 192) ? BT / 64 : (BT >= 128 ? 2 : 1);
   static constexpr int COLS = BT / EW;                     // token columns per epilogue WG
   static constexpr int CONV_WARP0 = 4 + 4 * EW;
   // weight-decode warps, in groups of eight (one thread per weight row and
@@ -158,13 +163,16 @@ struct Layout {
        (kind_f8w(KIND) && BT <= 32))
           ? 2
           : 1;
-  static constexpr int NCV = (KIND == KIND_F8F8) ? 0 : 8 * NDG;
+  // bf16 kinds: weight-decode warps; F8Q: one warpgroup quantizing the tokens
+  static constexpr int NCV = (KIND == KIND_F8F8) ? 0 : (KIND == KIND_F8Q ? 4 : 8 * NDG);
   static constexpr int kThreads = 128 * (1 + EW) + 32 * NCV;
   static constexpr int A_BYTES = kind_mx(KIND) ? 128 * 64 : 128 * 128;
-  static constexpr int B_BYTES = BT * 128 * ((KIND == KIND_F8F8) ? 1 : 2);
+  static constexpr int B_BYTES = BT * 128 * (kind_f8mma(KIND) ? 1 : 2);
+  // F8Q: the raw bf16 token slice of each stage (two 64-column halves)
+  static constexpr int X_BYTES = (KIND == KIND_F8Q) ? BT * 256 : 0;
   // bf16 kinds: decoded weight slices (128 rows x 128 K bf16 = 64 TMEM
   // columns each) live in a TMEM ring and feed the MMA's A operand directly
-  static constexpr int CS = (KIND == KIND_F8F8) ? 0 : 4;
+  static constexpr int CS = kind_f8mma(KIND) ? 0 : 4;
   static constexpr int C_TCOL = 256;                       // first column of that ring
   static constexpr int STG = EW >= 4 ? 8 : 16;             // token columns staged per pass
   // TMEM columns loaded per wait (bounded by registers: acc + one group
@@ -181,21 +189,21 @@ struct Layout {
   static constexpr int FIXED = OUT_BYTES + MISC_BYTES;
   // F8F8: A and B stages in lock step; bf16 kinds: B ring 4 deep when it fits
   static constexpr int BS_PREF =
-      (KIND == KIND_F8F8) ? 0 : (B_BYTES * 4 + 4 * A_BYTES + FIXED <= BUDGET ? 4 : 2);
+      kind_f8mma(KIND) ? 0 : (B_BYTES * 4 + 4 * A_BYTES + FIXED <= BUDGET ? 4 : 2);
   static constexpr int AS_RAW =
-      (KIND == KIND_F8F8) ? (BUDGET - FIXED) / (A_BYTES + B_BYTES)
+      kind_f8mma(KIND) ? (BUDGET - FIXED) / (A_BYTES + B_BYTES + X_BYTES)
                           : (BUDGET - FIXED - BS_PREF * B_BYTES) / A_BYTES;
   static constexpr int AS = AS_RAW > 12 ? 12 : AS_RAW;
-  static constexpr int BS = (KIND == KIND_F8F8) ? AS : BS_PREF;
-  static constexpr int TOTAL = AS * A_BYTES + BS * B_BYTES + OUT_BYTES + MISC_BYTES;
+  static constexpr int BS = kind_f8mma(KIND) ? AS : BS_PREF;
+  static constexpr int TOTAL = AS * A_BYTES + BS * B_BYTES + AS * X_BYTES + OUT_BYTES + MISC_BYTES;
   // TMEM accumulator buffers (the bf16 kinds keep columns 256.. for the
   // decoded-weight ring)
   static constexpr int NBUF = (BT > 128 || (KIND != KIND_F8F8 && BT == 128)) ? 2 : 4;
   // each accumulator starts at a power-of-two column offset (192-wide tiles
   // take 256-column slots); the allocation is a power of two
   static constexpr int BSTRIDE = BT > 128 ? 256 : BT;
-  static constexpr int TMEM_COLS = (KIND == KIND_F8F8) ? NBUF * BSTRIDE : 512;
-  static_assert(KIND == KIND_F8F8 || NBUF * BSTRIDE <= C_TCOL, "accumulators overlap the decode ring");
+  static constexpr int TMEM_COLS = kind_f8mma(KIND) ? NBUF * BSTRIDE : 512;
+  static_assert(kind_f8mma(KIND) || NBUF * BSTRIDE <= C_TCOL, "accumulators overlap the decode ring");
   static_assert(AS >= 2 && BS >= 2, "pipeline too shallow");
   static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory over budget");
   static_assert(COLS % 32 == 0 && COLS <= 128, "epilogue column split");
@@ -377,7 +385,7 @@ template <int KIND, int EPI, int BT, bool PROMOTE>
 __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   using L = Layout<KIND, BT, EPI>;
-  static_assert(KIND != KIND_F8F8 || PROMOTE, "FP8 x FP8 slices are always promoted (two issuers rely on it)");
+  static_assert(!kind_f8mma(KIND) || PROMOTE, "FP8 x FP8 slices are always promoted (two issuers rely on it)");
   static_assert(PROMOTE || L::STG == 16, "whole-K epilogue reads 16-column chunks");
   constexpr int AS = L::AS, BS = L::BS, CS = L::CS, EW = L::EW, COLS = L::COLS;
   constexpr int SSL = L::SSLOTS, STG = L::STG, GRP = L::GRP, NB = L::NBUF;
@@ -387,7 +395,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;
   uint8_t* sB = sA + AS * L::A_BYTES;
-  float* sOut = reinterpret_cast<float*>(sB + BS * L::B_BYTES);
+  uint8_t* sX = sB + BS * L::B_BYTES;    // F8Q raw token slices
+  float* sOut = reinterpret_cast<float*>(sX + AS * L::X_BYTES);
   uint8_t* misc = reinterpret_cast<uint8_t*>(sOut) + L::OUT_BYTES;
   uint64_t* a_full = reinterpret_cast<uint64_t*>(misc);
   uint64_t* a_empty = a_full + 12;
@@ -401,7 +410,12 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   uint64_t* s_empty = s_full + SSL;
   uint64_t* drain = s_empty + SSL;   // one per MMA issuer
   uint64_t* epi_bar = drain + 2;     // bounded barriers, one per epilogue warpgroup
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 4);
+  // F8Q: q_full[stage] (quantized B operand ready, on b_full), and the ring of
+  // token-group scales per slice, qs_full / qs_empty [8]
+  uint64_t* q_full = b_full;
+  uint64_t* qs_full = epi_bar + 4;
+  uint64_t* qs_empty = qs_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qs_empty + 8);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* sAsc = reinterpret_cast<float*>(misc + 1024);            // [SSL][BT] column scales
   float* sWr = reinterpret_cast<float*>(misc + 1024 + 8192);      // [SSL][128] row scales
@@ -409,6 +423,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   // sAsc for bf16 decode; its own area for f16 decode, whose slots also
   // carry column scales, BT <= 128)
   uint32_t* sMx = reinterpret_cast<uint32_t*>(misc + 1024);
+  // F8Q: [8][BT] token-group scales As(m, kb), slot = slice % 8
+  float* sQs = reinterpret_cast<float*>(misc + 1024 + 4096);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -419,11 +435,17 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < AS; ++i) {
       mbar_init(&a_full[i], 1);
-      mbar_init(&a_empty[i], KIND == KIND_F8F8 ? 1 : 8);   // one decode group per slice
+      mbar_init(&a_empty[i], kind_f8mma(KIND) ? 1 : 8);   // one decode group per slice
     }
     for (int i = 0; i < BS; ++i) {
-      mbar_init(&b_full[i], 1);
+      mbar_init(&b_full[i], KIND == KIND_F8Q ? 4 : 1);   // F8Q: q_full, the 4 quantizer warps
       mbar_init(&b_empty[i], 1);
+    }
+    if (KIND == KIND_F8Q) {
+      for (int i = 0; i < 8; ++i) {
+        mbar_init(&qs_full[i], 4);
+        mbar_init(&qs_empty[i], 4 * EW);
+      }
     }
     for (int i = 0; i < CS; ++i) {
       mbar_init(&c_full[i], 8);
@@ -502,6 +524,13 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
             // FP8 x FP8: both operands of the slice land on one barrier
             mbar_expect_tx(&a_full[s], L::A_BYTES + U.brows * 128);
             tma_load_2d(sB + s * L::B_BYTES, &maps.b[U.bvar], &a_full[s], kb * 128, U.brow);
+          } else if (KIND == KIND_F8Q) {
+            // weights and the bf16 token slice (two 64-column halves) on one
+            // barrier; the quantizer warps turn the tokens into the e4m3 B
+            mbar_expect_tx(&a_full[s], L::A_BYTES + U.brows * 256);
+            uint8_t* xd = sX + s * L::X_BYTES;
+            tma_load_2d(xd, &maps.b[U.bvar], &a_full[s], kb * 128, U.brow);
+            tma_load_2d(xd + U.brows * 128, &maps.b[U.bvar], &a_full[s], kb * 128 + 64, U.brow);
           } else {
             mbar_expect_tx(&a_full[s], L::A_BYTES);
           }
@@ -525,7 +554,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         const uint32_t first = it > static_cast<uint32_t>(AS) ? it - AS : 0;
         for (uint32_t i = first; i < it; ++i) mbar_wait(&a_full[i % AS], (i / AS) & 1, dw);
       }
-    } else if (lane == 1 && KIND != KIND_F8F8 && !p.inject_stall) {
+    } else if (lane == 1 && !kind_f8mma(KIND) && !p.inject_stall) {
       // bf16 kinds: the B operand (bf16 tokens, two 64-column halves) of
       // every slice, in slice order, into its own ring released by the MMA.
       // It runs apart from the scale loader so that the scale ring (which
@@ -576,7 +605,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         const int brows = U.brows;
         const int nsl = U.kb1 - U.kb0;
         const uint32_t idesc =
-            (KIND == KIND_F8F8) ? idesc_e4m3(128, U.n_inst)
+            kind_f8mma(KIND) ? idesc_e4m3(128, U.n_inst)
                                 : (kind_f16(KIND) ? idesc_f16(128, U.n_inst) : idesc_bf16(128, U.n_inst));
         uint32_t ubuf = 0;
         if (!PROMOTE) {
@@ -602,11 +631,12 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           if (PROMOTE)
             if (!mbar_wait_warp(&t_empty[buf], ((au / NB) & 1) ^ 1, wc)) goto mma_done;
           // FP8 x FP8 reads the A ring; the bf16 kinds read the decoded C ring
-          constexpr int RA = (KIND == KIND_F8F8) ? AS : CS;
+          constexpr int RA = kind_f8mma(KIND) ? AS : CS;
           const int sa = ia % RA;
-          uint64_t* full = (KIND == KIND_F8F8) ? &a_full[sa] : &c_full[sa];
+          uint64_t* full = kind_f8mma(KIND) ? &a_full[sa] : &c_full[sa];
           if (!mbar_wait_warp(full, (ia / RA) & 1, wc)) goto mma_done;
           const int sb = ib % BS;
+          // bf16 kinds: the token ring; F8Q: the quantized tokens of the stage
           if (KIND != KIND_F8F8)
             if (!mbar_wait_warp(&b_full[sb], (ib / BS) & 1, wc)) goto mma_done;
           tc_fence_after();
@@ -616,7 +646,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           first = false;
           const bool leader = elect_one();
           if (leader) {
-          if (KIND == KIND_F8F8) {
+          if (kind_f8mma(KIND)) {
             const uint32_t a0 = smem_u32(sA + sa * L::A_BYTES);
             const uint32_t b0 = smem_u32(sB + sb * L::B_BYTES);
 #pragma unroll
@@ -638,7 +668,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
             }
             mma_commit(&c_empty[sa]);
           }
-          if (KIND != KIND_F8F8) mma_commit(&b_empty[sb]);
+          if (!kind_f8mma(KIND)) mma_commit(&b_empty[sb]);
           }
           ++ia;
           ++ib;
@@ -792,7 +822,76 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     // its row's bytes from the (swizzled) shared tile, decodes them and
     // stores 32 columns of bf16 pairs into the TMEM ring slot, which the
     // MMA then reads as its A operand.
-    if constexpr (KIND != KIND_F8F8) {
+    if constexpr (KIND == KIND_F8Q) {
+      // --------------------------------------------- token quantization
+      // Thread = (token row j = t / 4 of the tile, quarter q4 = t % 4 of the
+      // slice's 128 K values).  Each 1 x 128 group is one K slice of a row:
+      // amax over the group, s = max(amax, eps) / 448 and codes
+      // e4m3(clamp(x / s, -448, 448)), both IEEE divisions, round to nearest
+      // even, exactly as the per_token_group_quant_fp8 kernel; the codes go to
+      // the slice's B stage in the 128-byte-swizzled layout the MMA reads,
+      // s to the scale ring the epilogue reads.
+      const int t = static_cast<int>(threadIdx.x) - L::CONV_WARP0 * 32;
+      const int j = t >> 2, q4 = t & 3;
+      uint32_t i = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit U = get_unit<EPI, BT>(p, u);
+        for (int kb = U.kb0; kb < U.kb1; ++kb, ++i) {
+          const int st = static_cast<int>(i % AS), qs = static_cast<int>(i % 8);
+          if (!mbar_wait(&a_full[st], (i / AS) & 1, wc)) goto quant_done;
+          if (!mbar_wait(&qs_empty[qs], ((i / 8) & 1) ^ 1, wc)) goto quant_done;
+          const bool valid = j < U.rows;
+          float v[32];
+          const uint8_t* xrow = sX + st * L::X_BYTES + (q4 >> 1) * (U.brows * 128) + j * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int chunk = 4 * (q4 & 1) + c;
+            const uint4 w = *reinterpret_cast<const uint4*>(xrow + ((chunk ^ (j & 7)) << 4));
+            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              v[8 * c + 2 * h] = __uint_as_float(wv[h] << 16);
+              v[8 * c + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
+            }
+          }
+          float amax = 0.f;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float a = fabsf(v[k]);
+            amax = (a > amax) ? a : amax;
+          }
+#pragma unroll
+          for (int off = 1; off <= 2; off <<= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, amax, off);
+            amax = (o > amax) ? o : amax;
+          }
+          const float sc = __fdiv_rn((amax > p.q_eps) ? amax : p.q_eps, 448.f);
+          uint32_t pk[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+          if (valid) {   // rows past the tile's tokens stay zero
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float* vv = v + 4 * k;
+              const uint16_t a = e4m3x2_rn(clamp448(__fdiv_rn(vv[0], sc)), clamp448(__fdiv_rn(vv[1], sc)));
+              const uint16_t b = e4m3x2_rn(clamp448(__fdiv_rn(vv[2], sc)), clamp448(__fdiv_rn(vv[3], sc)));
+              pk[k] = static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
+            }
+          }
+          uint8_t* brow = sB + st * L::B_BYTES + j * 128;
+          *reinterpret_cast<uint4*>(brow + (((2 * q4) ^ (j & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(brow + (((2 * q4 + 1) ^ (j & 7)) << 4)) =
+              make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          if (q4 == 0) sQs[qs * BT + j] = valid ? sc : 1.f;
+          // the codes are read by the tensor core (async proxy)
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&q_full[st]);
+            mbar_arrive(&qs_full[qs]);
+          }
+        }
+      }
+    quant_done:;
+    } else if constexpr (KIND != KIND_F8F8) {
       const int cw = warp - L::CONV_WARP0;
       const uint32_t grp = static_cast<uint32_t>(cw >> 3);   // takes slices with ia % NDG == grp
       const int half = (cw >> 2) & 1;
@@ -1069,8 +1168,13 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           const int slot = is % SSL;
           if (!mbar_wait(&s_full[slot], (is / SSL) & 1, wc)) goto epi_done;
           if (!mbar_wait(&t_full[buf], (au / NB) & 1, wc)) goto epi_done;
+          // F8Q: the slice's token-group scales come from the quantizer warps
+          const int qsl = static_cast<int>(is % 8);
+          if (KIND == KIND_F8Q)
+            if (!mbar_wait(&qs_full[qsl], (is / 8) & 1, wc)) goto epi_done;
           tc_fence_after();
           const float* sc = sAsc + slot * BT + col0;
+          const float* qsc = sQs + qsl * BT + col0;
           const float wr = lane_ws ? sWr[slot * 128 + et] : 1.f;
 #pragma unroll
           for (int c = 0; c < COLS / GRP; ++c) {
@@ -1096,7 +1200,11 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
               // packed fp32 FMA: two accumulator elements per instruction
 #pragma unroll
               for (int j = 0; j < GRP; j += 4) {
-                const float4 s4 = *reinterpret_cast<const float4*>(sc + c * GRP + j);
+                float4 s4 = *reinterpret_cast<const float4*>(sc + c * GRP + j);
+                if (KIND == KIND_F8Q) {
+                  const float4 q4v = *reinterpret_cast<const float4*>(qsc + c * GRP + j);
+                  s4 = make_float4(s4.x * q4v.x, s4.y * q4v.y, s4.z * q4v.z, s4.w * q4v.w);
+                }
                 float* a = acc + c * GRP + j;
                 const float2 lo = __ffma2_rn(make_float2(v[j], v[j + 1]), make_float2(s4.x, s4.y),
                                              make_float2(a[0], a[1]));
@@ -1115,7 +1223,10 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
             if (lane == 0) mbar_arrive(&t_empty[buf]);
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&s_empty[slot]);
+          if (lane == 0) {
+            mbar_arrive(&s_empty[slot]);
+            if (KIND == KIND_F8Q) mbar_arrive(&qs_empty[qsl]);
+          }
           ++au;
           ++is;
         }

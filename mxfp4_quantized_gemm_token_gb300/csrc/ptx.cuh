@@ -37,6 +37,21 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ------------------------------------------------ e4m3 quantization steps
+// clamp to the e4m3 range by comparisons (not fminf/fmaxf) so a NaN stays NaN
+__device__ __forceinline__ float clamp448(float t) {
+  t = (t > 448.f) ? 448.f : t;
+  t = (t < -448.f) ? -448.f : t;
+  return t;
+}
+
+// two fp32 -> two e4m3 codes (lo in the low byte), round to nearest even
+__device__ __forceinline__ uint16_t e4m3x2_rn(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // ------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

@@ -17,19 +17,6 @@
 
 namespace mxq {
 
-__device__ __forceinline__ float clamp448(float t) {
-  // comparisons (not fminf/fmaxf) so a NaN stays NaN
-  t = (t > 448.f) ? 448.f : t;
-  t = (t < -448.f) ? -448.f : t;
-  return t;
-}
-
-// two fp32 -> two e4m3 codes (lo in the low byte), round to nearest even
-__device__ __forceinline__ uint16_t e4m3x2_rn(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 
 // group == 128, K % 128 == 0, 16-byte aligned rows.  A warp takes 8 groups
 // per iteration (each half warp 4): all 4 loads of a lane are issued before
