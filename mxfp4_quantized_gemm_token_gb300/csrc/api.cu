@@ -250,15 +250,16 @@ MmPlan plan_mm(int64_t M, int64_t N, int64_t K, int32_t a_dtype, bool block, boo
   pl.bt = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
   const int64_t tile = option(MXQ_OPT_TILE_N);
   if (tile > 0) pl.bt = (tile == 256 && pl.kind != KIND_F8F8) ? 128 : static_cast<int>(tile);
-  // Large M with a weight scale that is uniform over 128 weight rows: put the
-  // tokens on the MMA M side so each TMEM lane's slice scale is one scalar.
-  pl.normal = pl.kind == KIND_F8F8 && has_ascale && uniform_wscale && M > 128 && tile == 0;
+  // Large M: put the tokens on the MMA M side (each TMEM lane's token scale
+  // is one scalar per slice; [1, 128] weight scales become a per-column
+  // vector the scale warp stages)
+  pl.normal = pl.kind == KIND_F8F8 && has_ascale && M > 128 && tile == 0;
   if (pl.normal) {
     const int64_t nt = option(MXQ_OPT_NORMAL_TILE);
     // 128-wide weight tiles: four TMEM accumulator buffers (one per slice in
     // flight) and two epilogue warpgroups of 64 columns; measured faster than
     // 192 (two buffers) and 256 (the epilogue spills) at M = 1024 and 4096
-    pl.bt = nt > 0 ? static_cast<int>(nt) : 128;
+    pl.bt = (nt > 0 && uniform_wscale) ? static_cast<int>(nt) : 128;
   }
   pl.promote = block || has_ascale;
   pl.tiles_n = static_cast<int>(cdiv(N, pl.normal ? pl.bt : 128));
@@ -475,7 +476,8 @@ mxq_status scaled_mm_run(const void* A, int32_t a_dtype, int64_t M, int64_t K, i
   const int64_t units = static_cast<int64_t>(pl.tiles_n) * pl.tiles_m * pl.splits;
   const int grid = static_cast<int>(std::min<int64_t>(units, sms));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_gemm(pl.kind, pl.normal ? EPI_NORMAL : EPI_DENSE, pl.bt, pl.promote,
+  const int epi = !pl.normal ? EPI_DENSE : (block_n == 1 ? EPI_NORMAL_COLW : EPI_NORMAL);
+  cudaError_t e = launch_gemm(pl.kind, epi, pl.bt, pl.promote,
                               maps, p, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "scaled-mm launch");
   if (pl.splits > 1) {

@@ -19,6 +19,12 @@ cudaError_t launch_gemm(int kind, int epi, int bt, bool promote, const GemmMaps&
       return launch_gemm_inst<KIND_F8F8, EPI_NORMAL, 256, true>(maps, p, grid, stream);
     return cudaErrorInvalidValue;
   }
+  if (epi == EPI_NORMAL_COLW) {
+    // tokens on the MMA M side with a weight scale per column ([1, 128] blocks)
+    if (kind == KIND_F8F8 && bt == 128)
+      return launch_gemm_inst<KIND_F8F8, EPI_NORMAL_COLW, 128, true>(maps, p, grid, stream);
+    return cudaErrorInvalidValue;
+  }
   if (epi != EPI_DENSE) return launch_gemm_moe(kind, epi, bt, promote, maps, p, grid, stream);
   if (kind == KIND_F8Q) {
     // decode-size W8A8 with the activation quantization inside the GEMM

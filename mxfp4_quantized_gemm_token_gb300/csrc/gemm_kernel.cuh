@@ -71,7 +71,10 @@ __host__ __device__ constexpr bool kind_f16(int k) { return k == KIND_F8H || k =
 // EPI_NORMAL: tokens on the MMA M side, weights on N (large M with uniform
 //             [128,128] / per-tensor weight scales: the slice scale is one
 //             scalar per TMEM lane, As(m, kb) * Ws(kb))
-enum { EPI_DENSE = 0, EPI_SILU = 1, EPI_SCATTER = 2, EPI_NORMAL = 3 };
+// EPI_NORMAL_COLW: the token-major orientation with one weight scale per
+//             column ([1, 128] weight blocks), staged per slice by the scale warp
+enum { EPI_DENSE = 0, EPI_SILU = 1, EPI_SCATTER = 2, EPI_NORMAL = 3, EPI_NORMAL_COLW = 4 };
+__host__ __device__ constexpr bool epi_normal(int e) { return e == EPI_NORMAL || e == EPI_NORMAL_COLW; }
 enum { DT_BF16 = 1, DT_F32 = 2 };
 
 struct GemmMaps {
@@ -178,11 +181,11 @@ struct Layout {
   // TMEM columns loaded per wait (bounded by registers: acc + one group
   // live).  The token-major epilogue at 512 threads reads its 64 columns with
   // one wait, so the accumulator buffer goes back to the MMA before any FMA.
-  static constexpr int GRP = (EPI == EPI_NORMAL && kThreads == 512)
+  static constexpr int GRP = (epi_normal(EPI) && kThreads == 512)
                                  ? 64
                                  : (kThreads >= 640 ? 16 : ((kThreads >= 512 || COLS > 64) ? 32 : COLS));
   // output staging of the weight-major epilogue (the token-major one stores directly)
-  static constexpr int OUT_BYTES = (EPI == EPI_NORMAL) ? 0 : EW * STG * 128 * 4;
+  static constexpr int OUT_BYTES = epi_normal(EPI) ? 0 : EW * STG * 128 * 4;
   static constexpr int SSLOTS = 8;                         // scale ring depth
   static constexpr int MISC_BYTES = 16384;
   static constexpr int BUDGET = 225 * 1024 - 1024;   // minus alignment slack
@@ -248,7 +251,7 @@ __device__ __forceinline__ Unit get_unit(const GemmParams& p, int u) {
     U.n_inst = BT;
     U.bvar = box_variant(BT);
     U.brows = BT;
-    if (EPI == EPI_NORMAL) {
+    if (epi_normal(EPI)) {
       // 128 tokens (A, TMEM lanes) x BT weight rows (B, TMEM columns)
       U.n0 = U.tn * BT;
       U.m0 = tm * 128;
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   }
   // (maps.a holds the weights in the weight-major orientation; prepacked
   // weights are read without a tensor map)
-  if (warp == 0 && lane == 0 && (EPI == EPI_NORMAL || p.wpacked == nullptr))
+  if (warp == 0 && lane == 0 && (epi_normal(EPI) || p.wpacked == nullptr))
     tma_prefetch_desc(&maps.a);
   if (warp == 1) {
     tmem_alloc(tmem_slot, L::TMEM_COLS);
@@ -492,7 +495,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     if (lane == 0 && !p.inject_stall) {
       // weights on the A side are streamed once: evict them first; tokens on
       // the A side (token-major path) are reused by every weight tile
-      const uint64_t pol = (EPI == EPI_NORMAL) ? policy_evict_last() : policy_evict_first();
+      const uint64_t pol = epi_normal(EPI) ? policy_evict_last() : policy_evict_first();
       uint32_t it = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
@@ -501,7 +504,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           if (!mbar_wait(&a_empty[s], ((it / AS) & 1) ^ 1, wc)) goto prod_a_done;
           const int kc = kind_mx(KIND) ? kb * 64 : kb * 128;
           uint8_t* dst = sA + s * L::A_BYTES;
-          if (EPI == EPI_NORMAL && p.wpacked != nullptr) {
+          if (epi_normal(EPI) && p.wpacked != nullptr) {
             // token-major with prepacked weights: the B operand (BT weight
             // rows of slice kb) is BT / 64 contiguous 8 KB halves of packed
             // tiles; halves past the padded row count are not loaded (their
@@ -534,7 +537,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           } else {
             mbar_expect_tx(&a_full[s], L::A_BYTES);
           }
-          if (EPI != EPI_NORMAL && EPI != EPI_SILU && p.wpacked != nullptr) {
+          if (!epi_normal(EPI) && EPI != EPI_SILU && p.wpacked != nullptr) {
             // weight-major with prepacked weights: one contiguous 16 KB tile
             bulk_load_hint(dst, p.wpacked + (static_cast<int64_t>(U.wrow0 >> 7) * p.nkb + kb) * 16384,
                            16384, &a_full[s], pol);
@@ -754,8 +757,45 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         }
       }
     mx_done:;
-    } else if (EPI == EPI_NORMAL) {
-      // token-major: the epilogue threads read their own slice scales
+    } else if (epi_normal(EPI)) {
+      // token-major: the epilogue threads read their own token scales; with
+      // per-row weight scales ([1, 128] blocks) the weight rows are the
+      // tile's columns, and this warp stages each slice's BT column scales
+      // Ws(n, kb) in the shared ring, four slices ahead
+      if (EPI == EPI_NORMAL_COLW) {
+        constexpr int NW = BT / 32;
+        uint32_t is = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+          const Unit U = get_unit<EPI, BT>(p, u);
+          float rw[4][NW];
+          auto fetch = [&](int kb, float* w) {
+#pragma unroll
+            for (int i = 0; i < NW; ++i) {
+              const int n = U.n0 + lane + 32 * i;
+              w[i] = n < p.N ? __ldg(p.w_scale + static_cast<int64_t>(n) * p.sw0 + kb * p.sw1) : 1.f;
+            }
+          };
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (U.kb0 + q < U.kb1) fetch(U.kb0 + q, rw[q]);
+          for (int kb = U.kb0; kb < U.kb1; kb += 4) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (kb + q < U.kb1) {
+                const int slot = is % SSL;
+                if (!mbar_wait(&s_empty[slot], ((is / SSL) & 1) ^ 1, wc)) goto ncol_done;
+#pragma unroll
+                for (int i = 0; i < NW; ++i) sAsc[slot * BT + lane + 32 * i] = rw[q][i];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_full[slot]);
+                ++is;
+                if (kb + q + 4 < U.kb1) fetch(kb + q + 4, rw[q]);
+              }
+            }
+          }
+        }
+      ncol_done:;
+      }
     } else if (PROMOTE) {
       // Four slices of look-ahead in registers hide the global-load latency.
       constexpr int NA = BT / 32;
@@ -1012,7 +1052,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       }
     conv_done:;
     }
-  } else if (warp >= 4 && EPI == EPI_NORMAL) {
+  } else if (warp >= 4 && epi_normal(EPI)) {
     // ------------------------------------- epilogue, tokens on TMEM lanes
     // Thread = token row m; its slice scale As(m, kb) * Ws(blk, kb) is one
     // scalar (a warpgroup's 64 columns lie in one 128-row weight block), so
@@ -1022,7 +1062,10 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     const int et = (threadIdx.x - 128) & 127;
     const int col0 = g * COLS;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t au = 0;
+    // [1, 128] weight blocks: a scale per column (weight row), staged per
+    // slice by the scale warp; the lane's token scale multiplies it
+    constexpr bool colw = EPI == EPI_NORMAL_COLW;
+    uint32_t au = 0, is = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit U = get_unit<EPI, BT>(p, u);
       const bool mrow = et < U.rows;
@@ -1037,14 +1080,14 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       // ahead; rows and blocks past the tile's valid ones read a valid entry
       const float* arow = p.a_scale + static_cast<int64_t>(U.m0 + min(et, U.rows - 1)) * p.sa0;
       const int wb = min((U.n0 + col0) / 128, (p.N - 1) / 128);
-      const float* wrow = p.w_scale + (p.block_n == 0 ? 0 : static_cast<int64_t>(wb) * p.sw0);
-      const int64_t wk = p.block_n == 0 ? 0 : p.sw1;
+      const float* wrow = p.w_scale + (p.block_n != 128 ? 0 : static_cast<int64_t>(wb) * p.sw0);
+      const int64_t wk = p.block_n != 128 ? 0 : p.sw1;
       float ra[4], rw[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int k = min(U.kb0 + q, U.kb1 - 1);
         ra[q] = __ldg(arow + k * p.sa1);
-        rw[q] = __ldg(wrow + k * wk);
+        rw[q] = colw ? 1.f : __ldg(wrow + k * wk);
       }
       for (int kb4 = U.kb0; kb4 < U.kb1; kb4 += 4)
 #pragma unroll
@@ -1054,12 +1097,15 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         const float sc = ra[q] * rw[q];
         if (kb + 4 < U.kb1) {
           ra[q] = __ldg(arow + (kb + 4) * p.sa1);
-          rw[q] = __ldg(wrow + (kb + 4) * wk);
+          rw[q] = colw ? 1.f : __ldg(wrow + (kb + 4) * wk);
         }
         const uint32_t buf = au % NB;
+        const int slot = is % SSL;
+        if (colw && !mbar_wait(&s_full[slot], (is / SSL) & 1, wc)) goto epin_done;
         if (!mbar_wait(&t_full[buf], (au / NB) & 1, wc)) goto epin_done;
         tc_fence_after();
         const float2 s2 = make_float2(sc, sc);
+        const float* wcol = sAsc + slot * BT + col0;
 #pragma unroll
         for (int c = 0; c < COLS / GRP; ++c) {
           if (c < ngr) {
@@ -1070,12 +1116,29 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(&t_empty[buf]);
             }
+            if (colw) {
+              // per column: As(m, kb) * Ws(n, kb), one packed multiply more
 #pragma unroll
-            for (int j = 0; j < GRP; j += 2) {
-              const float2 r = __ffma2_rn(make_float2(v[j], v[j + 1]), s2,
-                                          make_float2(acc[c * GRP + j], acc[c * GRP + j + 1]));
-              acc[c * GRP + j] = r.x;
-              acc[c * GRP + j + 1] = r.y;
+              for (int j = 0; j < GRP; j += 4) {
+                const float4 w4 = *reinterpret_cast<const float4*>(wcol + c * GRP + j);
+                const float2 lo = __fmul2_rn(make_float2(w4.x, w4.y), s2);
+                const float2 hi = __fmul2_rn(make_float2(w4.z, w4.w), s2);
+                float* a = acc + c * GRP + j;
+                const float2 r0 = __ffma2_rn(make_float2(v[j], v[j + 1]), lo, make_float2(a[0], a[1]));
+                const float2 r1 = __ffma2_rn(make_float2(v[j + 2], v[j + 3]), hi, make_float2(a[2], a[3]));
+                a[0] = r0.x;
+                a[1] = r0.y;
+                a[2] = r1.x;
+                a[3] = r1.y;
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < GRP; j += 2) {
+                const float2 r = __ffma2_rn(make_float2(v[j], v[j + 1]), s2,
+                                            make_float2(acc[c * GRP + j], acc[c * GRP + j + 1]));
+                acc[c * GRP + j] = r.x;
+                acc[c * GRP + j + 1] = r.y;
+              }
             }
           }
         }
@@ -1083,6 +1146,11 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&t_empty[buf]);
+        }
+        if (colw) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[slot]);
+          ++is;
         }
         ++au;
       }
