@@ -379,11 +379,28 @@ def run_profile(args, local):
 
 # ---------------------------------------------------------- other workloads
 
+class L2Flush:
+    """Evicts L2 before a timed call by reading a 512 MB buffer (4x L2).  A
+    read leaves only clean lines behind; a write flush would leave ~L2-size
+    dirty lines whose write-back then overlaps the timed call."""
+
+    def __init__(self, dev, mode="read"):
+        self.buf = torch.zeros(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+        self.acc = torch.zeros((), dtype=torch.float32, device=dev)
+        self.mode = mode
+
+    def __call__(self):
+        if self.mode == "write":
+            self.buf.zero_()
+        else:
+            torch.sum(self.buf, dim=0, out=self.acc)
+
+
 def _timed_calls(fn, reps, flush):
     """Median device time (ms) of fn() over reps calls, L2 flushed before each."""
     ts = []
     for _ in range(reps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fn()
@@ -476,13 +493,13 @@ def run_fp8_peak(local):
 def run_workloads(args, local):
     """One JSON line per shape of the other hot-path configurations (for the
     results tables): per-tensor W8A16, [1,128] block W8A8, fused MoE FP8-block
-    and MXFP4.  Each call is timed alone with L2 flushed (512 MB write) before it."""
+    and MXFP4.  Each call is timed alone with L2 flushed (a 512 MB read) before it."""
     import mxfp4_quantized_gemm_token_gb300 as mxq
     from mxfp4_quantized_gemm_token_gb300 import synth
     dev = torch.device("cuda", local)
     pk, _ = peaks()
     hbm = pk["hbm_gbs"]
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, args.flush)
     reps = args.steps
     names = args.workload.split(",")
     out = []
@@ -492,7 +509,27 @@ def run_workloads(args, local):
         print(json.dumps(d), flush=True)
 
     for name in names:
-        if name == "pertensor":
+        if name == "block128":
+            # the bench workload per M: the scaled GEMM alone on pre-quantized
+            # activations, and the whole linear (quantization + GEMM)
+            w, ws = synth.block_fp8_weight(18432, 7168, 128, seed=1, device=dev)
+            for M in (1, 8, 17, 128, 1024, 4096):
+                x = synth.activations(M, 7168, seed=M, device=dev)
+                qa, sa = mxq.per_token_group_quant_fp8(x, 128)
+                g = lambda: mxq.fp8_scaled_mm(qa, w, ws, [128, 128], a_scale=sa)
+                f = lambda: mxq.w8a8_block_fp8_linear(x, w, [128, 128], ws)
+                for _ in range(args.warmup):
+                    g()
+                    f()
+                gemm_ms = _timed_calls(g, reps, flush)
+                ms = _timed_calls(f, reps, flush)
+                byts = 18432 * 7168 + 144 * 56 * 4 + M * (7168 + 56 * 4) + M * 18432 * 2
+                flops = 2 * M * 18432 * 7168
+                emit({"M": M, "N": 18432, "K": 7168, "gemm_us": gemm_ms * 1e3, "linear_us": ms * 1e3,
+                      "gemm_TFLOPs": flops / gemm_ms / 1e9, "gemm_GBs": byts / gemm_ms / 1e6,
+                      "gemm_hbm_frac": byts / gemm_ms / 1e6 / hbm,
+                      "gemm_fp8_frac": flops / gemm_ms / 1e9 / (2.0 * pk["bf16_tflops"])})
+        elif name == "pertensor":
             a, w, scale, bias = synth.per_tensor_fp8_problem(seed=0)
             a, w, scale, bias = a.to(dev), w.to(dev), scale.to(dev), bias.to(dev)
             for _ in range(args.warmup):
@@ -513,13 +550,20 @@ def run_workloads(args, local):
                 else:
                     x = synth.activations(M, 7168, seed=M, device=dev)
                 f = lambda: mxq.w8a8_block_fp8_linear(x, w, [1, 128], ws)
+                qa, sa = mxq.per_token_group_quant_fp8(x, 128)
+                qf = lambda: mxq.per_token_group_quant_fp8(x, 128)
+                g = lambda: mxq.fp8_scaled_mm(qa, w, ws, [1, 128], a_scale=sa)
                 for _ in range(args.warmup):
                     f()
+                    g()
                 ms = _timed_calls(f, reps, flush)
                 gms = _graph_timed_calls(f, reps, flush)
+                gemm_ms = _timed_calls(g, reps, flush)
+                quant_ms = _timed_calls(qf, reps, flush)
                 byts = 4096 * 7168 + 4096 * 56 * 4 + M * 7168 * 2 + M * 4096 * 2
                 emit({"M": M, "N": 4096, "K": 7168, "us": ms * 1e3,
                       "us_graph": None if gms is None else gms * 1e3,
+                      "gemm_us": gemm_ms * 1e3, "quant_us": quant_ms * 1e3,
                       "TFLOPs": 2 * M * 4096 * 7168 / ms / 1e9, "GBs": byts / ms / 1e6,
                       "hbm_frac": byts / ms / 1e6 / hbm})
         elif name in ("moe_fp8", "moe_mxfp4"):
@@ -575,8 +619,9 @@ def run_ablation(args, local):
     import mxfp4_quantized_gemm_token_gb300 as mxq
     from mxfp4_quantized_gemm_token_gb300 import synth, _lib
     dev = torch.device("cuda", local)
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, args.flush)
     modes = (("per_block", 0), ("global", 3), ("all_narrow", 1), ("all_full", 2))
+    prev = mxq.get_option(_lib.OPT_SMALL_M_MAX)
     try:
         mxq.set_option(_lib.OPT_SMALL_M_MAX, 16)
         for kind in ("fp8", "mxfp4"):
@@ -612,7 +657,7 @@ def run_ablation(args, local):
                     print(json.dumps(line), flush=True)
     finally:
         mxq.set_option(_lib.OPT_FORCE_PATH, 0)
-        mxq.set_option(_lib.OPT_SMALL_M_MAX, 1 << 30)
+        mxq.set_option(_lib.OPT_SMALL_M_MAX, prev)
     return 0
 
 
@@ -628,13 +673,15 @@ def main():
     ap.add_argument("--fp8-peak", action="store_true",
                     help="measure the vendor FP8 GEMM burst rate (8192^3) and exit")
     ap.add_argument("--workload", default="",
-                    help="comma list of pertensor, block1x128, moe_fp8, moe_mxfp4 (tables only)")
+                    help="comma list of block128, pertensor, block1x128, moe_fp8, moe_mxfp4 (tables only)")
     ap.add_argument("--block-m", type=int, default=0,
                     help="MoE tokens per expert block; 0 = the library's choice")
     ap.add_argument("--profile", type=int, default=0,
                     help="run 3 launches of quant + GEMM at this M only (for ncu)")
     ap.add_argument("--profile-moe", default="",
                     help="kind:T:E, e.g. mxfp4:64:128 -- two fused-MoE calls (for ncu)")
+    ap.add_argument("--flush", default="read", choices=["read", "write"],
+                    help="L2 flush of the tables: read (default) or write a 512 MB buffer")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu DRAM bytes per launch of the dominant kernel (if measured)")
     args = ap.parse_args()

@@ -29,7 +29,7 @@ mxq_status cuda_fail(cudaError_t e, const char* what) {
   return fail(MXQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-std::atomic<int64_t> g_opts[13] = {0, 4, 0, 2000000000LL, 0, 0, 0, 0, 0, 1, 0, 1, 0};
+std::atomic<int64_t> g_opts[13] = {0, 4, 0, 2000000000LL, 0, 0, 0, 0, 0, 1, 0, 2, 0};
 
 std::mutex g_dev_mu;
 DeviceInfo g_devs[64];
@@ -854,8 +854,9 @@ MoeWs moe_ws(int64_t T, int64_t K, int32_t E, int64_t N, int32_t topk, int32_t b
   w.rs2 = o;
   o = round_up(o + static_cast<size_t>(w.S) * 4, 256);
   // MXFP4 with f16 operands: the largest scale exponent of every expert row
+  // (W1 rows, then W2 rows)
   w.emax = o;
-  o = round_up(o + static_cast<size_t>(E) * std::max<int64_t>(2 * N, K), 256);
+  o = round_up(o + static_cast<size_t>(E) * (2 * N + K), 256);
   w.total = o;
   return w;
 }
@@ -929,6 +930,12 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
     e = launch_rows_to_f16(hidden, T, K, ldh, nullptr, hf16, tscale, st);
     if (e != cudaSuccess) return cuda_fail(e, "token conversion launch");
   }
+  if (f16 && wtype == MXQ_W_MXFP4) {
+    // the f16 decode's per-row reference exponents of both expert matrices
+    e = launch_mx_row_emax(w1_scale, 2 * N, K / 32, K / 32, emax, w2_scale, K, N / 32, N / 32,
+                           emax + E * 2 * N, expert_ids, nblocks, E, w.cap, st);
+    if (e != cudaSuccess) return cuda_fail(e, "MXFP4 row exponent launch");
+  }
   e = launch_gather_rows(f16 ? hf16 : hidden, f16 ? K : ldh, K, topk, sorted_ids, offsets, nblocks,
                          block_m, w.cap, xs, fuse_combine ? cnt : nullptr, w.ncnt,
                          f16 ? tscale : nullptr, f16 ? rs1 : nullptr, st);
@@ -970,15 +977,18 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
                        CU_TENSOR_MAP_SWIZZLE_128B, &err))
         return fail(MXQ_ERR_CUDA, err);
     } else {
-      // 64-byte swizzle: the decode threads (one per weight row) read
-      // 16-byte chunks of 64-byte rows without bank conflicts
-      if (!make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, wt, red / 2, E * rows, red / 2, 64,
-                       arows, CU_TENSOR_MAP_SWIZZLE_64B, &err))
+      // boxes of 128-byte rows (two K slices of e2m1) with the 128-byte
+      // swizzle: the decode threads (one per weight row) read 16-byte chunks
+      // without bank conflicts
+      if (!make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, wt, red / 2, E * rows, red / 2, 128,
+                       arows, CU_TENSOR_MAP_SWIZZLE_128B, &err))
         return fail(MXQ_ERR_CUDA, err);
     }
-    for (int v = 0; v < 4; ++v) {
-      const uint32_t br = 16u << v;
-      if (static_cast<int>(br) > bt) break;
+    // token boxes of 16 / 32 / 64 / 128 rows, and (b[4]) 8 rows for expert
+    // blocks of at most 8 slots
+    for (int v = 0; v < 5; ++v) {
+      const uint32_t br = v == 4 ? 8u : 16u << v;
+      if (v < 4 && static_cast<int>(br) > bt) continue;
       if (!make_map_2d(&maps.b[v],
                        f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src,
                        red, w.S, red * 2, 64, br, CU_TENSOR_MAP_SWIZZLE_128B, &err))
@@ -1028,11 +1038,7 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
       p.sa0 = 1;
       p.sa1 = 0;
     }
-    if (kind == KIND_MXH) {
-      e = launch_mx_row_emax(wsc, rows, red / 32, red / 32, expert_ids, nblocks, E, w.cap, emax, st);
-      if (e != cudaSuccess) return cuda_fail(e, "MXFP4 row exponent launch");
-      p.mx_emax = emax;
-    }
+    if (kind == KIND_MXH) p.mx_emax = emax + (stage == 0 ? 0 : E * 2 * N);
     p.bias = stage == 0 ? w1_bias : w2_bias;
     p.bias_dtype = MXQ_F32;
     p.bias_e = rows;

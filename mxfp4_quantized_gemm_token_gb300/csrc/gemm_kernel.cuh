@@ -79,7 +79,7 @@ enum { DT_BF16 = 1, DT_F32 = 2 };
 
 struct GemmMaps {
   CUtensorMap a;      // weights; fp8 box [128 B x 128 (64 for SiLU) rows], e2m1x2 box [64 B x rows]
-  CUtensorMap b[5];   // tokens; box rows 16 / 32 / 64 / 128 / 256
+  CUtensorMap b[5];   // tokens; box rows 16 / 32 / 64 / 128 / 256 (grouped: b[4] 8 rows)
 };
 
 struct GemmParams {
@@ -169,14 +169,15 @@ struct Layout {
   // bf16 kinds: weight-decode warps; F8Q: one warpgroup quantizing the tokens
   static constexpr int NCV = (KIND == KIND_F8F8) ? 0 : (KIND == KIND_F8Q ? 4 : 8 * NDG);
   static constexpr int kThreads = 128 * (1 + EW) + 32 * NCV;
-  static constexpr int A_BYTES = kind_mx(KIND) ? 128 * 64 : 128 * 128;
+  // MXFP4: one A stage holds two consecutive K slices of a unit, loaded as
+  // 128-byte rows (K 256); the TMA streams 128-byte rows about 1.5x faster
+  // than 64-byte ones.  A unit with an odd slice count ends on a stage with
+  // one slice (the box's other half is the zero fill past K).
+  static constexpr int A_PER = kind_mx(KIND) ? 2 : 1;      // K slices per A stage
+  static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = BT * 128 * (kind_f8mma(KIND) ? 1 : 2);
   // F8Q: the raw bf16 token slice of each stage (two 64-column halves)
   static constexpr int X_BYTES = (KIND == KIND_F8Q) ? BT * 256 : 0;
-  // bf16 kinds: decoded weight slices (128 rows x 128 K bf16 = 64 TMEM
-  // columns each) live in a TMEM ring and feed the MMA's A operand directly
-  static constexpr int CS = kind_f8mma(KIND) ? 0 : 4;
-  static constexpr int C_TCOL = 256;                       // first column of that ring
   static constexpr int STG = EW >= 4 ? 8 : 16;             // token columns staged per pass
   // TMEM columns loaded per wait (bounded by registers: acc + one group
   // live).  The token-major epilogue at 512 threads reads its 64 columns with
@@ -190,7 +191,7 @@ struct Layout {
   static constexpr int MISC_BYTES = 16384;
   static constexpr int BUDGET = 225 * 1024 - 1024;   // minus alignment slack
   static constexpr int FIXED = OUT_BYTES + MISC_BYTES;
-  // F8F8: A and B stages in lock step; bf16 kinds: B ring 4 deep when it fits
+  // F8F8: A and B stages in lock step; bf16 kinds: the B ring 4 deep when it fits
   static constexpr int BS_PREF =
       kind_f8mma(KIND) ? 0 : (B_BYTES * 4 + 4 * A_BYTES + FIXED <= BUDGET ? 4 : 2);
   static constexpr int AS_RAW =
@@ -205,9 +206,23 @@ struct Layout {
   // each accumulator starts at a power-of-two column offset (192-wide tiles
   // take 256-column slots); the allocation is a power of two
   static constexpr int BSTRIDE = BT > 128 ? 256 : BT;
+  // bf16 kinds: decoded weight slices (128 rows x 128 K bf16 = 64 TMEM
+  // columns each) live in a TMEM ring after the accumulators and feed the
+  // MMA's A operand directly: MXFP4 six slots when the accumulators leave
+  // room (tiles of up to 32 tokens), else four; an even count, so that each
+  // slot is filled by one decode group and read by one MMA issuer
+  static constexpr int C_TCOL = kind_f8mma(KIND) ? 256 : (NBUF * BSTRIDE < 128 ? 128 : NBUF * BSTRIDE);
+  static constexpr int CS_RAW = (512 - C_TCOL) / 64;
+  static constexpr int CS = kind_f8mma(KIND) ? 0 : ((kind_mx(KIND) && CS_RAW >= 6) ? 6 : 4);
   static constexpr int TMEM_COLS = kind_f8mma(KIND) ? NBUF * BSTRIDE : 512;
-  static_assert(kind_f8mma(KIND) || NBUF * BSTRIDE <= C_TCOL, "accumulators overlap the decode ring");
+  static_assert(kind_f8mma(KIND) || (NBUF * BSTRIDE <= C_TCOL && C_TCOL + CS * 64 <= 512 && CS <= 8 &&
+                                     CS % 2 == 0),
+                "accumulators overlap the decode ring");
   static_assert(AS >= 2 && BS >= 2, "pipeline too shallow");
+  // two consumers take alternate slices of the A ring (decode groups, or the
+  // MMA issuers of FP8 x FP8): with three stages one of them can pass a
+  // parity wait a lap early (found by the CPU model of the ring protocol)
+  static_assert(AS >= 4 || (A_PER == 1 && NDG == 1 && !kind_f8mma(KIND)), "A ring too shallow");
   static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory over budget");
   static_assert(COLS % 32 == 0 && COLS <= 128, "epilogue column split");
   static_assert(SSLOTS * BT * 4 <= 8192, "scale ring size");
@@ -226,7 +241,9 @@ struct Unit {
   int brow;           // TMA row coordinate of the MMA-B box
   int n_inst;   // MMA instruction N
   int bvar;     // MMA-B box variant (maps.b[bvar])
-  int brows;    // rows of that box
+  int brows;    // rows of that box (the B tile's rows in shared memory)
+  int lvar;     // box variant the tokens are loaded with (maps.b[lvar])
+  int lrows;    // rows it loads (<= brows; rows past it are never stored)
 };
 
 __device__ __forceinline__ int box_variant(int n) {
@@ -251,6 +268,8 @@ __device__ __forceinline__ Unit get_unit(const GemmParams& p, int u) {
     U.n_inst = BT;
     U.bvar = box_variant(BT);
     U.brows = BT;
+    U.lvar = U.bvar;
+    U.lrows = BT;
     if (epi_normal(EPI)) {
       // 128 tokens (A, TMEM lanes) x BT weight rows (B, TMEM columns)
       U.n0 = U.tn * BT;
@@ -292,6 +311,12 @@ __device__ __forceinline__ Unit get_unit(const GemmParams& p, int u) {
     U.n_inst = (U.rows <= p.narrow_max) ? min(fit, BT) : BT;
     U.bvar = box_variant(U.n_inst);
     U.brows = 16 << U.bvar;
+    // a block of at most 8 slots loads 8 token rows: the MMA's other 8 rows
+    // of B hold stale data that only feeds accumulator columns past the
+    // block, which are never stored (token tiles share the TMA engine with
+    // the weight stream)
+    U.lvar = (U.n_inst == 16 && U.rows <= 8) ? 4 : U.bvar;
+    U.lrows = (U.n_inst == 16 && U.rows <= 8) ? 8 : U.brows;
     U.brow = U.m0;
   }
   return U;
@@ -374,6 +399,20 @@ __device__ __forceinline__ uint32_t f16_pow2(int d) {
   return d >= -14 ? static_cast<uint32_t>(d + 15) << 10 : (d >= -24 ? 1u << (d + 24) : 0u);
 }
 
+// MXFP4: the two ue8m0 bytes (low byte first) of 32-groups 2*half and
+// 2*half + 1 of slice kb in the scale row srow; 2^0 past the unit's slices
+// and past K (the weights there are zero)
+__device__ __forceinline__ uint32_t mx_scale2(const GemmParams& p, const uint8_t* srow, int kb,
+                                              int kb1, int half) {
+  const int col = kb * 4 + 2 * half;
+  if (kb >= kb1 || col >= p.mx_cols) return 0x7F7Fu;
+  if (p.mx_align >= 2 && col + 2 <= p.mx_cols)
+    return __ldg(reinterpret_cast<const uint16_t*>(srow + col));
+  const uint32_t b0 = __ldg(srow + col);
+  const uint32_t b1 = (col + 1 < p.mx_cols) ? __ldg(srow + col + 1) : 127u;
+  return b0 | (b1 << 8);
+}
+
 // Barrier of the 128 epilogue threads on an mbarrier, so that it is bounded
 // like every other wait (a plain bar.sync would hang if one warp gave up).
 __device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, const WaitCtx& w) {
@@ -406,8 +445,8 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   uint64_t* b_full = a_empty + 12;
   uint64_t* b_empty = b_full + 12;
   uint64_t* c_full = b_empty + 12;
-  uint64_t* c_empty = c_full + 4;
-  uint64_t* t_full = c_empty + 4;
+  uint64_t* c_empty = c_full + 8;
+  uint64_t* t_full = c_empty + 8;
   uint64_t* t_empty = t_full + 4;
   uint64_t* s_full = t_empty + 4;
   uint64_t* s_empty = s_full + SSL;
@@ -422,10 +461,6 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* sAsc = reinterpret_cast<float*>(misc + 1024);            // [SSL][BT] column scales
   float* sWr = reinterpret_cast<float*>(misc + 1024 + 8192);      // [SSL][128] row scales
-  // MXFP4: [SSL][128] ue8m0 bytes of one slice, 4 per weight row (shares
-  // sAsc for bf16 decode; its own area for f16 decode, whose slots also
-  // carry column scales, BT <= 128)
-  uint32_t* sMx = reinterpret_cast<uint32_t*>(misc + 1024);
   // F8Q: [8][BT] token-group scales As(m, kb), slot = slice % 8
   float* sQs = reinterpret_cast<float*>(misc + 1024 + 4096);
 
@@ -438,7 +473,9 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < AS; ++i) {
       mbar_init(&a_full[i], 1);
-      mbar_init(&a_empty[i], kind_f8mma(KIND) ? 1 : 8);   // one decode group per slice
+      // the MMA (FP8-MMA kinds) or the eight warps of the decode group of
+      // each slice of the stage (twice over for a stage with one slice)
+      mbar_init(&a_empty[i], kind_f8mma(KIND) ? 1 : 8 * L::A_PER);
     }
     for (int i = 0; i < BS; ++i) {
       mbar_init(&b_full[i], KIND == KIND_F8Q ? 4 : 1);   // F8Q: q_full, the 4 quantizer warps
@@ -491,65 +528,72 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
                               : p.tiles_n * p.tiles_m * p.splits * max(1, p.batch);
 
   if (warp == 0) {
-    // ------------------------------------------------ weight producer
+    // ------------------------------------------------ operand producer
     if (lane == 0 && !p.inject_stall) {
       // weights on the A side are streamed once: evict them first; tokens on
       // the A side (token-major path) are reused by every weight tile
       const uint64_t pol = epi_normal(EPI) ? policy_evict_last() : policy_evict_first();
+      // the copies of slice kb of unit U (MXFP4: slices kb and kb + 1) into
+      // A stage s (with the tokens too for the FP8-MMA kinds, which fill
+      // both operands on one barrier)
+      auto issue_a = [&](int s, const Unit& U, int kb) {
+        const int kc = kind_mx(KIND) ? kb * 64 : kb * 128;
+        uint8_t* dst = sA + s * L::A_BYTES;
+        if (epi_normal(EPI) && p.wpacked != nullptr) {
+          // token-major with prepacked weights: the B operand (BT weight
+          // rows of slice kb) is BT / 64 contiguous 8 KB halves of packed
+          // tiles; halves past the padded row count are not loaded (their
+          // accumulator columns are never stored)
+          uint32_t bytes = L::A_BYTES;
+#pragma unroll
+          for (int c = 0; c < BT / 64; ++c)
+            if (U.brow + 64 * c < p.npad) bytes += 8192;
+          mbar_expect_tx(&a_full[s], bytes);
+#pragma unroll
+          for (int c = 0; c < BT / 64; ++c) {
+            const int row = U.brow + 64 * c;
+            if (row < p.npad)
+              bulk_load(sB + s * L::B_BYTES + c * 8192,
+                        p.wpacked + (static_cast<int64_t>(row >> 7) * p.nkb + kb) * 16384 +
+                            ((row >> 6) & 1) * 8192,
+                        8192, &a_full[s]);
+          }
+        } else if (KIND == KIND_F8F8) {
+          // FP8 x FP8: both operands of the slice land on one barrier
+          mbar_expect_tx(&a_full[s], L::A_BYTES + U.brows * 128);
+          tma_load_2d(sB + s * L::B_BYTES, &maps.b[U.bvar], &a_full[s], kb * 128, U.brow);
+        } else if (KIND == KIND_F8Q) {
+          // weights and the bf16 token slice (two 64-column halves) on one
+          // barrier; the quantizer warps turn the tokens into the e4m3 B
+          mbar_expect_tx(&a_full[s], L::A_BYTES + U.brows * 256);
+          uint8_t* xd = sX + s * L::X_BYTES;
+          tma_load_2d(xd, &maps.b[U.bvar], &a_full[s], kb * 128, U.brow);
+          tma_load_2d(xd + U.brows * 128, &maps.b[U.bvar], &a_full[s], kb * 128 + 64, U.brow);
+        } else {
+          mbar_expect_tx(&a_full[s], L::A_BYTES);
+        }
+        if (!epi_normal(EPI) && EPI != EPI_SILU && p.wpacked != nullptr) {
+          // weight-major with prepacked weights: one contiguous 16 KB tile
+          bulk_load_hint(dst, p.wpacked + (static_cast<int64_t>(U.wrow0 >> 7) * p.nkb + kb) * 16384,
+                         16384, &a_full[s], pol);
+        } else if (EPI == EPI_SILU) {
+          tma_load_2d_hint(dst, &maps.a, &a_full[s], kc, U.wrow0, pol);
+          tma_load_2d_hint(dst + L::A_BYTES / 2, &maps.a, &a_full[s], kc, U.wrow1, pol);
+        } else {
+          tma_load_2d_hint(dst, &maps.a, &a_full[s], kc, U.wrow0, pol);
+        }
+      };
+      // (lane 1 fills the token ring of the bf16 / f16 kinds)
       uint32_t it = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
-        for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
+        for (int kb = U.kb0; kb < U.kb1; kb += L::A_PER, ++it) {
           const int s = it % AS;
-          if (!mbar_wait(&a_empty[s], ((it / AS) & 1) ^ 1, wc)) goto prod_a_done;
-          const int kc = kind_mx(KIND) ? kb * 64 : kb * 128;
-          uint8_t* dst = sA + s * L::A_BYTES;
-          if (epi_normal(EPI) && p.wpacked != nullptr) {
-            // token-major with prepacked weights: the B operand (BT weight
-            // rows of slice kb) is BT / 64 contiguous 8 KB halves of packed
-            // tiles; halves past the padded row count are not loaded (their
-            // accumulator columns are never stored)
-            uint32_t bytes = L::A_BYTES;
-#pragma unroll
-            for (int c = 0; c < BT / 64; ++c)
-              if (U.brow + 64 * c < p.npad) bytes += 8192;
-            mbar_expect_tx(&a_full[s], bytes);
-#pragma unroll
-            for (int c = 0; c < BT / 64; ++c) {
-              const int row = U.brow + 64 * c;
-              if (row < p.npad)
-                bulk_load(sB + s * L::B_BYTES + c * 8192,
-                          p.wpacked + (static_cast<int64_t>(row >> 7) * p.nkb + kb) * 16384 +
-                              ((row >> 6) & 1) * 8192,
-                          8192, &a_full[s]);
-            }
-          } else if (KIND == KIND_F8F8) {
-            // FP8 x FP8: both operands of the slice land on one barrier
-            mbar_expect_tx(&a_full[s], L::A_BYTES + U.brows * 128);
-            tma_load_2d(sB + s * L::B_BYTES, &maps.b[U.bvar], &a_full[s], kb * 128, U.brow);
-          } else if (KIND == KIND_F8Q) {
-            // weights and the bf16 token slice (two 64-column halves) on one
-            // barrier; the quantizer warps turn the tokens into the e4m3 B
-            mbar_expect_tx(&a_full[s], L::A_BYTES + U.brows * 256);
-            uint8_t* xd = sX + s * L::X_BYTES;
-            tma_load_2d(xd, &maps.b[U.bvar], &a_full[s], kb * 128, U.brow);
-            tma_load_2d(xd + U.brows * 128, &maps.b[U.bvar], &a_full[s], kb * 128 + 64, U.brow);
-          } else {
-            mbar_expect_tx(&a_full[s], L::A_BYTES);
-          }
-          if (!epi_normal(EPI) && EPI != EPI_SILU && p.wpacked != nullptr) {
-            // weight-major with prepacked weights: one contiguous 16 KB tile
-            bulk_load_hint(dst, p.wpacked + (static_cast<int64_t>(U.wrow0 >> 7) * p.nkb + kb) * 16384,
-                           16384, &a_full[s], pol);
-          } else if (EPI == EPI_SILU) {
-            tma_load_2d_hint(dst, &maps.a, &a_full[s], kc, U.wrow0, pol);
-            tma_load_2d_hint(dst + L::A_BYTES / 2, &maps.a, &a_full[s], kc, U.wrow1, pol);
-          } else {
-            tma_load_2d_hint(dst, &maps.a, &a_full[s], kc, U.wrow0, pol);
-          }
+          if (!mbar_wait(&a_empty[s], ((it / AS) & 1) ^ 1, wc)) goto prod_done;
+          issue_a(s, U, kb);
         }
       }
-    prod_a_done:
+    prod_done:
       if (*abort_flag) {
         // let every copy already issued land before the CTA goes away
         volatile int zero = 0;
@@ -558,21 +602,18 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
         for (uint32_t i = first; i < it; ++i) mbar_wait(&a_full[i % AS], (i / AS) & 1, dw);
       }
     } else if (lane == 1 && !kind_f8mma(KIND) && !p.inject_stall) {
-      // bf16 kinds: the B operand (bf16 tokens, two 64-column halves) of
-      // every slice, in slice order, into its own ring released by the MMA.
-      // It runs apart from the scale loader so that the scale ring (which
-      // the MXFP4 decode waits on) is not held back by the B ring's depth.
+      // bf16 kinds: the B operand (bf16 / f16 tokens, two 64-column halves)
+      // of every slice, in slice order, into its own ring released by the MMA
       uint32_t itb = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
-        const CUtensorMap* mb = &maps.b[U.bvar];
         for (int kb = U.kb0; kb < U.kb1; ++kb, ++itb) {
           const int sb = itb % BS;
           if (!mbar_wait(&b_empty[sb], ((itb / BS) & 1) ^ 1, wc)) goto prod_b_done;
           uint8_t* dst = sB + sb * L::B_BYTES;
-          mbar_expect_tx(&b_full[sb], U.brows * 256);
-          tma_load_2d(dst, mb, &b_full[sb], kb * 128, U.brow);
-          tma_load_2d(dst + U.brows * 128, mb, &b_full[sb], kb * 128 + 64, U.brow);
+          mbar_expect_tx(&b_full[sb], U.lrows * 256);
+          tma_load_2d(dst, &maps.b[U.lvar], &b_full[sb], kb * 128, U.brow);
+          tma_load_2d(dst + U.brows * 128, &maps.b[U.lvar], &b_full[sb], kb * 128 + 64, U.brow);
         }
       }
     prod_b_done:
@@ -699,64 +740,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
     if (KIND == KIND_F8W && !PROMOTE) {
       // per-tensor weights: no slice scales
     } else if (kind_mx(KIND)) {
-      // ue8m0 bytes of each slice (4 groups of 32 along K per weight row),
-      // MLA slices ahead in registers; rows of a ragged tail clamp to the
-      // last row and columns past K read 127 (2^0; the data there is zero).
-      // With even row strides a row's four bytes are two 16-bit loads whose
-      // halves are joined only when the slice is published, so no fetch
-      // waits on its loads; other strides and a ragged K end join the bytes
-      // at once.
-      constexpr int MLA = 4;
-      uint32_t is = 0;
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const Unit U = get_unit<EPI, BT>(p, u);
-        uint32_t rh[MLA][8];
-        auto fetch = [&](int kb, uint32_t* h) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = lane + 32 * i;
-            int64_t grow = (EPI == EPI_SILU) ? static_cast<int64_t>(r < 64 ? U.wrow0 + r : U.wrow1 + (r - 64))
-                                             : static_cast<int64_t>(U.wrow0) + r;
-            if (grow >= p.mx_rows_total) grow = p.mx_rows_total - 1;
-            const uint8_t* rowp = p.mx_scale + grow * p.mx_ld + kb * 4;
-            if (p.mx_align >= 2 && kb * 4 + 4 <= p.mx_cols) {
-              const uint16_t* hp = reinterpret_cast<const uint16_t*>(rowp);
-              h[2 * i] = __ldg(hp);
-              h[2 * i + 1] = __ldg(hp + 1);
-            } else {
-              uint32_t v = 0;
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const int col = kb * 4 + c;
-                const uint32_t b = (col < p.mx_cols) ? __ldg(rowp + c) : 127u;
-                v |= b << (8 * c);
-              }
-              h[2 * i] = v & 0xFFFFu;
-              h[2 * i + 1] = v >> 16;
-            }
-          }
-        };
-#pragma unroll
-        for (int q = 0; q < MLA; ++q)
-          if (U.kb0 + q < U.kb1) fetch(U.kb0 + q, rh[q]);
-        for (int kb = U.kb0; kb < U.kb1; kb += MLA) {
-#pragma unroll
-          for (int q = 0; q < MLA; ++q) {
-            if (kb + q < U.kb1) {
-              const int slot = is % SSL;
-              if (!mbar_wait(&s_empty[slot], ((is / SSL) & 1) ^ 1, wc)) goto mx_done;
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                sMx[slot * 128 + lane + 32 * i] = rh[q][2 * i] | (rh[q][2 * i + 1] << 16);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&s_full[slot]);
-              ++is;
-              if (kb + q + MLA < U.kb1) fetch(kb + q + MLA, rh[q]);
-            }
-          }
-        }
-      }
-    mx_done:;
+      // MXFP4: the decode threads load their own ue8m0 bytes
     } else if (epi_normal(EPI)) {
       // token-major: the epilogue threads read their own token scales; with
       // per-row weight scales ([1, 128] blocks) the weight rows are the
@@ -938,23 +922,40 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       const int r = (warp & 3) * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
                              L::C_TCOL + half * 32;
-      uint32_t ia = 0, ic = 0, is = 0;
+      uint32_t ia = 0, ic = 0;
+      uint32_t sbase = 0;   // A stages of the CTA's earlier units
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit U = get_unit<EPI, BT>(p, u);
+        const int nsl = U.kb1 - U.kb0;
         int emax = 0;   // MXH: the row's largest scale exponent (the f16 reference)
-        if (KIND == KIND_MXH) {
+        // MXFP4: this thread's scale bytes, loaded by the thread itself two
+        // of its slices ahead (sq0: the next slice it decodes, sq1: the one
+        // after), so that no slice waits on a hand-off from another warp
+        const uint8_t* srow = nullptr;
+        uint32_t sq0 = 0, sq1 = 0;
+        if (kind_mx(KIND)) {
           int64_t grow = (EPI == EPI_SILU) ? static_cast<int64_t>(r < 64 ? U.wrow0 + r : U.wrow1 + (r - 64))
                                            : static_cast<int64_t>(U.wrow0) + r;
           if (grow >= p.mx_rows_total) grow = p.mx_rows_total - 1;
-          emax = __ldg(p.mx_emax + grow);
+          if (KIND == KIND_MXH) emax = __ldg(p.mx_emax + grow);
+          srow = p.mx_scale + grow * p.mx_ld;
+          // the unit's first slice of this group: kb0 + ((grp - ia) mod NDG)
+          const int kf = U.kb0 + static_cast<int>((grp + L::NDG - ia % L::NDG) % L::NDG);
+          sq0 = mx_scale2(p, srow, kf, U.kb1, half);
+          sq1 = mx_scale2(p, srow, kf + L::NDG, U.kb1, half);
         }
         for (int kb = U.kb0; kb < U.kb1; ++kb, ++ia, ++ic) {
-          if (L::NDG > 1 && ia % L::NDG != grp) {
-            if (kind_mx(KIND)) ++is;   // the other group's scale slot
-            continue;
-          }
-          const int sa = ia % AS, sc = ic % CS;
-          if (!mbar_wait(&a_full[sa], (ia / AS) & 1, wc)) goto conv_done;
+          if (L::NDG > 1 && ia % L::NDG != grp) continue;
+          // A stage of the slice (MXFP4: two slices of the unit per stage,
+          // slice half h in bytes 64h .. 64h+63 of each 128-byte row)
+          const int l = kb - U.kb0;
+          const uint32_t sta = sbase + static_cast<uint32_t>(l / L::A_PER);
+          const int h = l % L::A_PER;
+          // the stage's only slice (odd unit length): its decode group
+          // arrives for both halves
+          const bool single = L::A_PER == 2 && l == nsl - 1 && (nsl & 1);
+          const int sa = static_cast<int>(sta % AS), sc = ic % CS;
+          if (!mbar_wait(&a_full[sa], (sta / AS) & 1, wc)) goto conv_done;
           if (!mbar_wait(&c_empty[sc], ((ic / CS) & 1) ^ 1, wc)) goto conv_done;
           tc_fence_after();
           const uint8_t* src = sA + sa * L::A_BYTES;
@@ -982,28 +983,27 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
               }
             }
           } else {
-            // 64 e2m1 of row r: 16-byte chunks 2*half, 2*half+1 of the
-            // 64-byte row (64-byte swizzle); chunk c is the 32-group with
-            // ue8m0 scale byte c of the slice
-            const int slot = is % SSL;
-            if (!mbar_wait(&s_full[slot], (is / SSL) & 1, wc)) goto conv_done;
-            const uint32_t e4 = sMx[slot * 128 + r];
+            // 64 e2m1 of row r: 16-byte chunks 4h + 2*half, 4h + 2*half + 1
+            // of the 128-byte row (128-byte swizzle); chunk 2*half + k of
+            // the slice is the 32-group with ue8m0 scale byte 2*half + k
+            const uint32_t e2 = sq0;   // bytes of groups 2*half, 2*half + 1
+            sq0 = sq1;
+            sq1 = mx_scale2(p, srow, kb + 2 * L::NDG, U.kb1, half);
             uint4 raw[2];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-              const int c = 2 * half + k;
-              raw[k] = *reinterpret_cast<const uint4*>(src + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+              const int c = 4 * h + 2 * half + k;
+              raw[k] = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
             }
             __syncwarp();
             if (lane == 0) {
               mbar_arrive(&a_empty[sa]);
-              mbar_arrive(&s_empty[slot]);
+              if (single) mbar_arrive(&a_empty[sa]);
             }
-            ++is;
             if (KIND == KIND_MXH) {
 #pragma unroll
               for (int k = 0; k < 2; ++k) {
-                const int e = static_cast<int>((e4 >> (8 * (2 * half + k))) & 0xFFu);
+                const int e = static_cast<int>((e2 >> (8 * k)) & 0xFFu);
                 const uint32_t f2 = f16_pow2(e - emax) * 0x10001u;
                 const uint32_t in[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
@@ -1012,7 +1012,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
             } else
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-              const uint32_t e = (e4 >> (8 * (2 * half + k))) & 0xFFu;
+              const uint32_t e = (e2 >> (8 * k)) & 0xFFu;
               // bf16 2^(e - 127 + 112) when representable; else two steps
               __nv_bfloat162 sc2;
               uint32_t two_step = 0;
@@ -1049,6 +1049,7 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&c_full[sc]);
         }
+        sbase += static_cast<uint32_t>((nsl + L::A_PER - 1) / L::A_PER);
       }
     conv_done:;
     }

@@ -92,9 +92,10 @@ cudaError_t launch_gather_rows(const void* hidden, int64_t ldh, int64_t K, int32
                                int* zero, int64_t nzero, const float* tscale, float* rscale,
                                cudaStream_t stream);
 
-cudaError_t launch_mx_row_emax(const void* scales, int64_t rows, int64_t ncols, int64_t ld,
+cudaError_t launch_mx_row_emax(const void* s1, int64_t rows1, int64_t ncols1, int64_t ld1, void* e1,
+                               const void* s2, int64_t rows2, int64_t ncols2, int64_t ld2, void* e2,
                                const int32_t* expert_ids, const int32_t* num_blocks, int E,
-                               int64_t cap, void* emax, cudaStream_t stream);
+                               int64_t cap, cudaStream_t stream);
 
 cudaError_t launch_rows_to_f16(const void* src, int64_t rows, int64_t K, int64_t ld,
                                const int32_t* count, void* dst, float* rscale,

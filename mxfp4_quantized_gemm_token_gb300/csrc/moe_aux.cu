@@ -2,6 +2,7 @@
 // alignment, the token-row gather that feeds stage 1, the top-k combine, and
 // the small helpers (split-K reduction of fp8_scaled_mm, debug unsort).
 #include <cuda_bf16.h>
+#include <algorithm>
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -249,41 +250,73 @@ cudaError_t launch_rows_to_f16(const void* src, int64_t rows, int64_t K, int64_t
 // ------------------------------------------------ MXFP4 row exponents
 // The f16 decode of MXFP4 expert weights scales every 32-group relative to
 // the largest ue8m0 exponent of its weight row: emax[e * rows + r] = max over
-// k of scales[(e * rows + r) * ld + k].  Only the experts of the block table
-// are visited (a block whose expert repeats the previous block's is
-// skipped); one warp per row.
-__global__ void mx_row_emax_kernel(const uint8_t* __restrict__ scales, int64_t rows, int ncols,
-                                   int64_t ld, const int32_t* __restrict__ expert_ids,
-                                   const int32_t* __restrict__ num_blocks, int E,
-                                   uint8_t* __restrict__ emax) {
+// k of scales[(e * rows + r) * ld + k], for both expert matrices in one
+// launch.  Only the experts of the block table are visited (a block whose
+// expert repeats the previous block's is skipped).  CTA (block b, chunk c):
+// chunks [0, ch1) cover the rows of matrix 1 and [ch1, ch1 + ch2) those of
+// matrix 2, 256 rows each; one thread per row reads the row with the widest
+// loads its alignment allows (align: 4, 2 or 1 bytes for both matrices).
+namespace {
+
+__device__ __forceinline__ unsigned row_max_u8(const uint8_t* row, int ncols, int align) {
+  unsigned m = 0;
+  int c = 0;
+  if (align >= 4) {
+    for (; c + 4 <= ncols; c += 4) {
+      const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(row + c));
+      m = max(m, max(max(v & 0xFFu, (v >> 8) & 0xFFu), max((v >> 16) & 0xFFu, v >> 24)));
+    }
+  } else if (align >= 2) {
+    for (; c + 2 <= ncols; c += 2) {
+      const uint32_t v = __ldg(reinterpret_cast<const uint16_t*>(row + c));
+      m = max(m, max(v & 0xFFu, v >> 8));
+    }
+  }
+  for (; c < ncols; ++c) m = max(m, static_cast<unsigned>(__ldg(row + c)));
+  return m;
+}
+
+__global__ void __launch_bounds__(256) mx_row_emax_kernel(
+    const uint8_t* __restrict__ s1, int64_t rows1, int ncols1, int64_t ld1, uint8_t* __restrict__ e1,
+    const uint8_t* __restrict__ s2, int64_t rows2, int ncols2, int64_t ld2, uint8_t* __restrict__ e2,
+    int align, const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ num_blocks,
+    int E, int64_t ch1, int64_t ch2) {
   pdl_wait();
   pdl_launch_dependents();
-  const int nb = __ldg(num_blocks);
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       w < static_cast<int64_t>(nb) * rows; w += nwarps) {
-    const int b = static_cast<int>(w / rows);
-    const int64_t r = w - static_cast<int64_t>(b) * rows;
-    const int e = __ldg(expert_ids + b);
-    if (e < 0 || e >= E || (b > 0 && __ldg(expert_ids + b - 1) == e)) continue;
-    const uint8_t* row = scales + (static_cast<int64_t>(e) * rows + r) * ld;
-    unsigned m = 0;
-    for (int k = lane; k < ncols; k += 32) m = max(m, static_cast<unsigned>(__ldg(row + k)));
-    m = __reduce_max_sync(0xffffffffu, m);
-    if (lane == 0) emax[static_cast<int64_t>(e) * rows + r] = static_cast<uint8_t>(m);
+  const int b = blockIdx.x;
+  if (b >= __ldg(num_blocks)) return;
+  const int e = __ldg(expert_ids + b);
+  if (e < 0 || e >= E || (b > 0 && __ldg(expert_ids + b - 1) == e)) return;
+  for (int64_t c = blockIdx.y; c < ch1 + ch2; c += gridDim.y) {
+    const bool second = c >= ch1;
+    const int64_t rows = second ? rows2 : rows1;
+    const int64_t r = (second ? c - ch1 : c) * 256 + threadIdx.x;
+    if (r >= rows) continue;
+    const uint8_t* base = second ? s2 : s1;
+    const int64_t ld = second ? ld2 : ld1;
+    const unsigned m = row_max_u8(base + (static_cast<int64_t>(e) * rows + r) * ld,
+                                  second ? ncols2 : ncols1, align);
+    (second ? e2 : e1)[static_cast<int64_t>(e) * rows + r] = static_cast<uint8_t>(m);
   }
 }
 
-cudaError_t launch_mx_row_emax(const void* scales, int64_t rows, int64_t ncols, int64_t ld,
+}  // namespace
+
+cudaError_t launch_mx_row_emax(const void* s1, int64_t rows1, int64_t ncols1, int64_t ld1, void* e1,
+                               const void* s2, int64_t rows2, int64_t ncols2, int64_t ld2, void* e2,
                                const int32_t* expert_ids, const int32_t* num_blocks, int E,
-                               int64_t cap, void* emax, cudaStream_t stream) {
-  int64_t blocks = (cap * rows + 7) / 8;
-  if (blocks > 8192) blocks = 8192;
-  if (blocks < 1) blocks = 1;
-  return launch_k(mx_row_emax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
-                  reinterpret_cast<const uint8_t*>(scales), rows, static_cast<int>(ncols), ld,
-                  expert_ids, num_blocks, E, reinterpret_cast<uint8_t*>(emax));
+                               int64_t cap, cudaStream_t stream) {
+  if (cap <= 0) return cudaSuccess;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(s1) | reinterpret_cast<uintptr_t>(s2) |
+                      static_cast<uintptr_t>(ld1) | static_cast<uintptr_t>(ld2);
+  const int align = (a & 3) == 0 ? 4 : ((a & 1) == 0 ? 2 : 1);
+  const int64_t ch1 = (rows1 + 255) / 256, ch2 = (rows2 + 255) / 256;
+  const unsigned gy = static_cast<unsigned>(std::min<int64_t>(ch1 + ch2, 65535));
+  return launch_k(mx_row_emax_kernel, dim3(static_cast<unsigned>(cap), gy), dim3(256), 0, stream,
+                  reinterpret_cast<const uint8_t*>(s1), rows1, static_cast<int>(ncols1), ld1,
+                  reinterpret_cast<uint8_t*>(e1), reinterpret_cast<const uint8_t*>(s2), rows2,
+                  static_cast<int>(ncols2), ld2, reinterpret_cast<uint8_t*>(e2), align, expert_ids,
+                  num_blocks, E, ch1, ch2);
 }
 
 // ------------------------------------------------------------ row gather

@@ -171,9 +171,11 @@ def test_fused_narrow_and_wide_paths_agree(oracle, N, K):
         mxq.set_option(_lib.OPT_SMALL_M_MAX, old)
 
 
-def test_fused_mxfp4_scales_beyond_bf16_single_step(oracle):
+@pytest.mark.parametrize("mode", [1, 2])
+def test_fused_mxfp4_scales_beyond_bf16_single_step(oracle, mode):
     """ue8m0 exponents of 143 and above (scales of 2^16 and more, which the
-    decode folds into the bf16 weights in two multiplications) in stage 1,
+    bf16 decode, mode 1, folds into the weights in two multiplications and
+    the f16 decode, mode 2, applies as the row's fp32 factor) in stage 1,
     and small ones in stage 2, against the oracle, with the stage
     accumulators checked too."""
     E, N, K, T, topk = 4, 128, 256, 9, 2
@@ -184,6 +186,27 @@ def test_fused_mxfp4_scales_beyond_bf16_single_step(oracle):
     b1, b2 = synth.moe_biases(E, N, K, seed=52)
     x = synth.activations(T, K, seed=53, scale_div=10)
     tw, ids = synth.routing_uniform(T, E, topk, seed=54)
+    try:
+        mxq.set_option(_lib.OPT_MOE_F16, mode)
+        run_moe(oracle, W_MX, E, N, K, x, tw, ids, 16, wts=(w1, s1, w2, s2, b1, b2))
+    finally:
+        mxq.set_option(_lib.OPT_MOE_F16, 2)
+
+
+def test_fused_mxfp4_f16_decode_wide_exponent_spread(oracle):
+    """The f16 decode scales each 32-group by 2^(e - emax of its weight row):
+    every row's first group gets an exponent 20 above the rest but zero
+    codes, so the whole result comes from groups 2^20 below the row's
+    reference, which must stay exact (within 2^23 of it)."""
+    E, N, K, T, topk = 4, 128, 256, 9, 2
+    w1, s1, w2, s2 = synth.moe_mxfp4_weights(E, N, K, seed=61)
+    w1, s1, w2, s2 = w1.clone(), s1.clone(), w2.clone(), s2.clone()
+    for w, sc in ((w1, s1), (w2, s2)):
+        w[..., :16] = 0                                     # group 0: all codes zero
+        sc[..., 0] = (sc[..., 1:].to(torch.int32).amax(dim=-1) + 20).clamp(max=254).to(torch.uint8)
+    b1, b2 = synth.moe_biases(E, N, K, seed=62)
+    x = synth.activations(T, K, seed=63, scale_div=10)
+    tw, ids = synth.routing_uniform(T, E, topk, seed=64)
     run_moe(oracle, W_MX, E, N, K, x, tw, ids, 16, wts=(w1, s1, w2, s2, b1, b2))
 
 
@@ -220,12 +243,13 @@ def test_fused_combine_is_bit_identical_to_the_combine_kernel(oracle, wtype, T, 
     assert torch.equal(outs[0], outs[1])
 
 
-@pytest.mark.parametrize("mode", [0, 2])
+@pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("wtype,block_m", [(W_FP8, 32), (W_MX, 32), (W_FP8, 64), (W_MX, 64)])
 def test_fused_operand_modes(oracle, mode, wtype, block_m):
     """The expert GEMMs with bf16 operands (mode 0) and with f16 operands for
-    both weight formats (mode 2), against the oracle with the checkpoints and
-    the stage-accumulator probes (the default mode 1 runs everywhere else)."""
+    FP8 experts only (mode 1), against the oracle with the checkpoints and
+    the stage-accumulator probes (the default mode 2, f16 for both weight
+    formats, runs everywhere else)."""
     E, N, K, T, topk = 12, 256, 384, 40, 4
     x = synth.activations(T, K, seed=91, scale_div=10)
     tw, ids = synth.routing_zipf(T, E, topk, seed=92)
@@ -233,4 +257,4 @@ def test_fused_operand_modes(oracle, mode, wtype, block_m):
         mxq.set_option(_lib.OPT_MOE_F16, mode)
         run_moe(oracle, wtype, E, N, K, x, tw, ids, block_m, bias=(wtype == W_MX))
     finally:
-        mxq.set_option(_lib.OPT_MOE_F16, 1)
+        mxq.set_option(_lib.OPT_MOE_F16, 2)

@@ -14,9 +14,13 @@ check that every accumulator the epilogue reads holds exactly the unit's
 slices, and that nothing deadlocks.
 
 Roles modelled, per CTA (names as in the kernel):
-  producer      fills the A ring (weights) in slice order
+  producer      fills the A ring (weights) in slice order; an MXFP4 stage
+                holds two consecutive slices of one unit (one copy), and a
+                unit of odd length ends on a stage with one slice, whose
+                decode group arrives on the stage's empty barrier twice
   B producer    fills the B ring (bf16 tokens) in slice order (bf16 kinds)
-  scale loader  fills the scale ring in slice order (MXFP4)
+  scale loader  fills the scale ring in slice order (promoted kinds; the
+                MXFP4 decode threads load their own scale bytes)
   decode warps  NDG groups; group g decodes the slices with ia % NDG == g
                 into the C ring (TMEM); each warp arrives on its own
   MMA issuers   two; each takes alternate slices and commits asynchronously
@@ -63,7 +67,8 @@ class Cta:
     """State and roles of one persistent CTA processing `units` (slice counts)."""
 
     def __init__(self, units, promote, ndg, mxw, AS=12, BS=4, CS=4, SSL=8, NB=4,
-                 old_issuer_rule=False, warps_per_group=2, f8f8=False, scale_ring=True):
+                 old_issuer_rule=False, warps_per_group=2, f8f8=False, scale_ring=True,
+                 a_per=None, double_arrival=True):
         # f8f8: FP8 x FP8 (dense and token-major W8A8): one producer loads both
         # operands of a slice into the A ring, which the MMA issuers read
         # directly; the scale ring feeds the promotion epilogue; no decode
@@ -79,14 +84,17 @@ class Cta:
         self.old = old_issuer_rule
         self.wpg = warps_per_group
         W = warps_per_group
+        # K slices per A stage: two for MXFP4 (as the kernel), else one
+        self.a_per = a_per if a_per is not None else (2 if mxw else 1)
+        self.double_arrival = double_arrival
         self.a_full = [Bar("a_full%d" % i, 1) for i in range(AS)]
-        self.a_empty = [Bar("a_empty%d" % i, 1 if f8f8 else W) for i in range(AS)]
+        self.a_empty = [Bar("a_empty%d" % i, 1 if f8f8 else W * self.a_per) for i in range(AS)]
         self.b_full = [Bar("b_full%d" % i, 1) for i in range(BS)]
         self.b_empty = [Bar("b_empty%d" % i, 1) for i in range(BS)]
         self.c_full = [Bar("c_full%d" % i, W) for i in range(CS)]
         self.c_empty = [Bar("c_empty%d" % i, 1) for i in range(CS)]
         self.s_full = [Bar("s_full%d" % i, 1) for i in range(SSL)]
-        self.s_empty = [Bar("s_empty%d" % i, 1 if promote else W) for i in range(SSL)]
+        self.s_empty = [Bar("s_empty%d" % i, 1) for i in range(SSL)]
         self.t_full = [Bar("t_full%d" % i, 1) for i in range(NB)]
         self.t_empty = [Bar("t_empty%d" % i, 1) for i in range(NB)]
         # slot contents: which slice a slot holds, and how far it was consumed
@@ -102,19 +110,30 @@ class Cta:
         self.events = []                # asynchronous completions: (order key, fn)
         self.mma_queue = {0: [], 1: []} # per issuer, completions in issue order
         self.nslices = sum(units)
+        # A stages: a_per consecutive slices of one unit each
+        self.stages, self.stage_of = [], {}
+        base = 0
+        for nsl in units:
+            for l in range(0, nsl, self.a_per):
+                sl = tuple(range(base + l, base + min(nsl, l + self.a_per)))
+                for h, ia in enumerate(sl):
+                    self.stage_of[ia] = (len(self.stages), h, len(sl))
+                self.stages.append(sl)
+            base += nsl
 
     # ------------------------------------------------------------- roles
     def producer_a(self):
-        for it in range(self.nslices):
-            s = it % self.AS
-            yield self.a_empty[s], ((it // self.AS) & 1) ^ 1
-            check(it < self.AS or (self.a_slot[s] == it - self.AS and
-                                   self.a_reads[s] == (1 if self.f8f8 else self.wpg)),
-                  "A slot %d refilled for slice %d before slice %s was read by every decode warp"
-                  % (s, it, self.a_slot[s]))
+        for st, sl in enumerate(self.stages):
+            s = st % self.AS
+            yield self.a_empty[s], ((st // self.AS) & 1) ^ 1
+            check(st < self.AS or (self.a_slot[s] == self.stages[st - self.AS] and
+                                   self.a_reads[s] == (1 if self.f8f8 else self.wpg * self.a_per)),
+                  "A stage %d refilled with slices %s before slices %s were read by every "
+                  "decode warp" % (s, sl, self.a_slot[s]))
+            self.a_reads[s] = 0
 
-            def fill(s=s, it=it):
-                self.a_slot[s], self.a_reads[s] = it, 0
+            def fill(s=s, sl=sl):
+                self.a_slot[s] = sl
                 self.a_full[s].arrive()
             self.events.append(fill)
 
@@ -135,7 +154,7 @@ class Cta:
             s = i % self.SSL
             yield self.s_empty[s], ((i // self.SSL) & 1) ^ 1
             check(i < self.SSL or (self.s_slot[s] == i - self.SSL and
-                                   self.s_reads[s] == (1 if self.epi_scales else self.wpg)),
+                                   self.s_reads[s] == 1),
                   "scale slot %d republished before its slice was read" % s)
             self.s_slot[s], self.s_reads[s] = i, 0
             self.s_full[s].arrive()
@@ -144,22 +163,19 @@ class Cta:
         for ia in range(self.nslices):
             if ia % self.ndg != grp:
                 continue
-            sa, sc = ia % self.AS, ia % self.CS
-            yield self.a_full[sa], (ia // self.AS) & 1
-            check(self.a_slot[sa] == ia, "decode of slice %d read A slot %d holding slice %s"
-                  % (ia, sa, self.a_slot[sa]))
+            st, h, n = self.stage_of[ia]
+            sa, sc = st % self.AS, ia % self.CS
+            yield self.a_full[sa], (st // self.AS) & 1
+            check(self.a_slot[sa] is not None and len(self.a_slot[sa]) > h and
+                  self.a_slot[sa][h] == ia,
+                  "decode of slice %d read A stage %d holding slices %s" % (ia, sa, self.a_slot[sa]))
             yield self.c_empty[sc], ((ia // self.CS) & 1) ^ 1
             check(self.c_used[sc], "decode of slice %d overwrote C slot %d (slice %s) before "
                   "the MMA read it" % (ia, sc, self.c_slot[sc][w]))
-            if self.mxw:
-                ss = ia % self.SSL
-                yield self.s_full[ss], (ia // self.SSL) & 1
-                check(self.s_slot[ss] == ia, "decode of slice %d read scales of slice %s"
-                      % (ia, self.s_slot[ss]))
-                self.s_reads[ss] += 1
-                self.s_empty[ss].arrive()
-            self.a_reads[sa] += 1
-            self.a_empty[sa].arrive()
+            arrivals = 2 if (n < self.a_per and self.double_arrival) else 1
+            for _ in range(arrivals):
+                self.a_reads[sa] += 1
+                self.a_empty[sa].arrive()
             yield None                                  # the decode itself
             self.c_slot[sc][w] = ia
             if all(v == ia for v in self.c_slot[sc]):
@@ -193,8 +209,8 @@ class Cta:
                 if self.f8f8:
                     sa = ia % self.AS
                     yield self.a_full[sa], (ia // self.AS) & 1
-                    check(self.a_slot[sa] == ia, "MMA of slice %d read A slot %d holding slice %s"
-                          % (ia, sa, self.a_slot[sa]))
+                    check(self.a_slot[sa] is not None and self.a_slot[sa][0] == ia,
+                          "MMA of slice %d read A slot %d holding slice %s" % (ia, sa, self.a_slot[sa]))
 
                     def done(sa=sa, buf=buf, ia=ia):
                         self.acc[buf] = [ia]
@@ -280,7 +296,7 @@ class Cta:
         actors = [self.producer_a(), self.issuer(0), self.issuer(1), self.epilogue()]
         if not self.f8f8:
             actors.append(self.producer_b())     # bf16 tokens
-        if self.mxw or self.epi_scales:
+        if self.epi_scales:
             actors.append(self.scale_loader())
         for g in range(self.ndg):
             for w in range(self.wpg):
@@ -329,13 +345,41 @@ UNIT_PATTERNS = {
 @pytest.mark.parametrize("pattern", sorted(UNIT_PATTERNS))
 @pytest.mark.parametrize("kind", ["mxfp4_whole_k", "fp8_block_promoted", "per_tensor_whole_k"])
 @pytest.mark.parametrize("ndg", [1, 2])
-def test_ring_protocol_holds_under_random_interleavings(pattern, kind, ndg):
+@pytest.mark.parametrize("AS,BS,CS", [(12, 4, 4), (8, 8, 6), (4, 8, 4), (5, 4, 6)])
+def test_ring_protocol_holds_under_random_interleavings(pattern, kind, ndg, AS, BS, CS):
     units = UNIT_PATTERNS[pattern]
     promote = kind == "fp8_block_promoted"
     mxw = kind == "mxfp4_whole_k"
     for seed in range(40):
-        cta = Cta(units, promote=promote, ndg=ndg, mxw=mxw)
+        cta = Cta(units, promote=promote, ndg=ndg, mxw=mxw, AS=AS, BS=BS, CS=CS)
         cta.run(random.Random(seed))
+
+
+def test_model_finds_the_lap_behind_read_of_a_three_stage_ring():
+    """Two consumers taking alternate slices of one ring (the two decode
+    groups, or the two MMA issuers of FP8 x FP8) with only three stages: a
+    consumer can wait on a stage whose previous fill (the other consumer's
+    slice) has not landed, and its parity wait passes one lap early.  The
+    kernel's rings are four stages deep or more (asserted at compile time)."""
+    found = 0
+    for pat in UNIT_PATTERNS:
+        for seed in range(100):
+            try:
+                Cta(UNIT_PATTERNS[pat], promote=True, ndg=2, mxw=False, AS=3, BS=8).run(random.Random(seed))
+            except Violation:
+                found += 1
+    assert found > 0
+
+
+def test_model_finds_a_missing_second_arrival_of_a_one_slice_stage():
+    """MXFP4 stages of two slices of a unit: a unit of odd length ends on a
+    stage with one slice.  Without its decode group's second arrival on the
+    stage's empty barrier, the producer never gets the stage back, and the
+    model reports the deadlock."""
+    units = UNIT_PATTERNS["odd"]
+    with pytest.raises(Violation, match="deadlock"):
+        Cta(units, promote=False, ndg=2, mxw=True, AS=4, double_arrival=False).run(random.Random(0))
+    Cta(units, promote=False, ndg=2, mxw=True, AS=4).run(random.Random(0))
 
 
 def test_model_finds_the_stale_read_of_the_per_unit_issuer_rule():
