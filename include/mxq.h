@@ -100,9 +100,11 @@ enum {
                                GEMM (the last of a token's slots to finish a weight tile sums
                                its rows, ascending k); 0 (default, measured faster on GB300):
                                a separate combine kernel.  Bit-identical results either way. */
-  MXQ_OPT_MOE_F16 = 11,     /* fused MoE operand type: 2 (default) f16 for both expert
-                               formats; 1 f16 for FP8-block experts, bf16 for MXFP4; 0 bf16
-                               for both.  With f16 the
+  MXQ_OPT_MOE_F16 = 11,     /* fused MoE operand type: 3 (default) f16 for FP8-block
+                               experts, and for MXFP4 when T * topk > 16 (below, the f16
+                               path's extra launches cost more than its decode saves);
+                               2 f16 for both formats; 1 f16 for FP8-block experts, bf16
+                               for MXFP4; 0 bf16 for both.  With f16 the
                                expert GEMMs multiply f16 operands:
                                weights decode to f16 in one conversion per pair (MXFP4
                                groups scaled by 2^(e - emax of their weight row), the row's

@@ -29,7 +29,7 @@ mxq_status cuda_fail(cudaError_t e, const char* what) {
   return fail(MXQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-std::atomic<int64_t> g_opts[13] = {0, 4, 0, 2000000000LL, 0, 0, 0, 0, 0, 1, 0, 2, 0};
+std::atomic<int64_t> g_opts[13] = {0, 4, 0, 2000000000LL, 0, 0, 0, 0, 0, 1, 0, 3, 0};
 
 std::mutex g_dev_mu;
 DeviceInfo g_devs[64];
@@ -915,7 +915,11 @@ mxq_status fused_experts_impl(const void* hidden, int64_t T, int64_t K, int64_t 
   const bool fuse_combine = option(MXQ_OPT_FUSE_COMBINE) != 0;
   int* cnt = reinterpret_cast<int*>(ws + w.cnt);
   const int64_t f16_opt = option(MXQ_OPT_MOE_F16);
-  const bool f16 = f16_opt == 2 || (f16_opt == 1 && wtype == MXQ_W_FP8_BLOCK128);
+  // f16 operands: 2 both formats, 1 FP8 only, 3 (default) FP8 always and
+  // MXFP4 above 16 routed slots (below, its three extra launches cost more
+  // than the cheaper decode saves)
+  const bool f16 = f16_opt == 2 || (f16_opt == 1 && wtype == MXQ_W_FP8_BLOCK128) ||
+                   (f16_opt == 3 && (wtype == MXQ_W_FP8_BLOCK128 || w.S > 16));
   void* hf16 = ws + w.hf16;
   float* tscale = reinterpret_cast<float*>(ws + w.tscale);
   float* rs1 = reinterpret_cast<float*>(ws + w.rs1);

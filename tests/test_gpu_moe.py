@@ -190,7 +190,7 @@ def test_fused_mxfp4_scales_beyond_bf16_single_step(oracle, mode):
         mxq.set_option(_lib.OPT_MOE_F16, mode)
         run_moe(oracle, W_MX, E, N, K, x, tw, ids, 16, wts=(w1, s1, w2, s2, b1, b2))
     finally:
-        mxq.set_option(_lib.OPT_MOE_F16, 2)
+        mxq.set_option(_lib.OPT_MOE_F16, 3)
 
 
 def test_fused_mxfp4_f16_decode_wide_exponent_spread(oracle):
@@ -207,7 +207,11 @@ def test_fused_mxfp4_f16_decode_wide_exponent_spread(oracle):
     b1, b2 = synth.moe_biases(E, N, K, seed=62)
     x = synth.activations(T, K, seed=63, scale_div=10)
     tw, ids = synth.routing_uniform(T, E, topk, seed=64)
-    run_moe(oracle, W_MX, E, N, K, x, tw, ids, 16, wts=(w1, s1, w2, s2, b1, b2))
+    try:
+        mxq.set_option(_lib.OPT_MOE_F16, 2)
+        run_moe(oracle, W_MX, E, N, K, x, tw, ids, 16, wts=(w1, s1, w2, s2, b1, b2))
+    finally:
+        mxq.set_option(_lib.OPT_MOE_F16, 3)
 
 
 @pytest.mark.parametrize("wtype", [W_FP8, W_MX])
@@ -243,13 +247,13 @@ def test_fused_combine_is_bit_identical_to_the_combine_kernel(oracle, wtype, T, 
     assert torch.equal(outs[0], outs[1])
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("wtype,block_m", [(W_FP8, 32), (W_MX, 32), (W_FP8, 64), (W_MX, 64)])
 def test_fused_operand_modes(oracle, mode, wtype, block_m):
-    """The expert GEMMs with bf16 operands (mode 0) and with f16 operands for
-    FP8 experts only (mode 1), against the oracle with the checkpoints and
-    the stage-accumulator probes (the default mode 2, f16 for both weight
-    formats, runs everywhere else)."""
+    """The expert GEMMs with bf16 operands (mode 0), f16 operands for FP8
+    experts only (mode 1) and f16 for both formats (mode 2), against the
+    oracle with the checkpoints and the stage-accumulator probes (the
+    default mode 3 runs everywhere else)."""
     E, N, K, T, topk = 12, 256, 384, 40, 4
     x = synth.activations(T, K, seed=91, scale_div=10)
     tw, ids = synth.routing_zipf(T, E, topk, seed=92)
@@ -257,4 +261,4 @@ def test_fused_operand_modes(oracle, mode, wtype, block_m):
         mxq.set_option(_lib.OPT_MOE_F16, mode)
         run_moe(oracle, wtype, E, N, K, x, tw, ids, block_m, bias=(wtype == W_MX))
     finally:
-        mxq.set_option(_lib.OPT_MOE_F16, 2)
+        mxq.set_option(_lib.OPT_MOE_F16, 3)
