@@ -146,8 +146,8 @@ extern "C" mxq_status mxq_set_option(int32_t opt, int64_t value) {
   if ((opt == MXQ_OPT_PDL || opt == MXQ_OPT_FUSE_COMBINE || opt == MXQ_OPT_FUSE_QUANT) &&
       value != 0 && value != 1)
     return fail(MXQ_ERR_INVALID_ARG, "PDL, FUSE_COMBINE and FUSE_QUANT are 0 (off) or 1 (on)");
-  if (opt == MXQ_OPT_MOE_F16 && value > 2)
-    return fail(MXQ_ERR_INVALID_ARG, "MOE_F16 is 0, 1 or 2");
+  if (opt == MXQ_OPT_MOE_F16 && value > 3)
+    return fail(MXQ_ERR_INVALID_ARG, "MOE_F16 is 0, 1, 2 or 3");
   if (opt == MXQ_OPT_FORCE_PATH && value > 3)
     return fail(MXQ_ERR_INVALID_ARG,
                 "FORCE_PATH is 0 (per block), 1 (narrow), 2 (full width) or 3 (one path per layer)");
