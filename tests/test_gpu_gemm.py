@@ -262,6 +262,15 @@ def test_per_row_weight_scales_large_m(oracle, seed):
                bias=torch.randn(200, generator=torch.Generator().manual_seed(seed)))
 
 
+@pytest.mark.parametrize("M,N,K", [(260, 392, 2400), (140, 136, 4224)])
+def test_per_row_weight_scales_chunk_tails(oracle, M, N, K):
+    """[1,128] weight scales on the token-major tiles with K slice counts of
+    19 and 33: the column scales are staged in chunks of 16 slices, so both
+    shapes end on a partial chunk (the first with a ragged K tail as well)."""
+    block_case(oracle, M, N, K, 1, seed=M + K,
+               bias=torch.randn(N, generator=torch.Generator().manual_seed(K)))
+
+
 @pytest.mark.parametrize("tile", [32, 64, 128, 256])
 def test_forced_token_tile_widths(oracle, tile):
     """Every token-tile width (MMA N and epilogue split) on a ragged shape."""
