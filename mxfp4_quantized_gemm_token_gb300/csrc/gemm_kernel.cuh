@@ -189,13 +189,8 @@ struct Layout {
   static constexpr int OUT_BYTES = epi_normal(EPI) ? 0 : EW * STG * 128 * 4;
   static constexpr int SSLOTS = 8;                         // scale ring depth
   static constexpr int MISC_BYTES = 16384;
-  // [1, 128] weight blocks, token-major: the column scales Ws(n, kb) of WCH
-  // consecutive slices of a tile are staged at once, in two chunk buffers,
-  // so the epilogue waits for them once per chunk rather than once per slice
-  static constexpr int WCH = 16;
-  static constexpr int WS_BYTES = EPI == EPI_NORMAL_COLW ? 2 * WCH * BT * 4 : 0;
   static constexpr int BUDGET = 225 * 1024 - 1024;   // minus alignment slack
-  static constexpr int FIXED = OUT_BYTES + MISC_BYTES + WS_BYTES;
+  static constexpr int FIXED = OUT_BYTES + MISC_BYTES;
   // F8F8: A and B stages in lock step; bf16 kinds: the B ring 4 deep when it fits
   static constexpr int BS_PREF =
       kind_f8mma(KIND) ? 0 : (B_BYTES * 4 + 4 * A_BYTES + FIXED <= BUDGET ? 4 : 2);
@@ -204,7 +199,7 @@ struct Layout {
                           : (BUDGET - FIXED - BS_PREF * B_BYTES) / A_BYTES;
   static constexpr int AS = AS_RAW > 12 ? 12 : AS_RAW;
   static constexpr int BS = kind_f8mma(KIND) ? AS : BS_PREF;
-  static constexpr int TOTAL = AS * A_BYTES + BS * B_BYTES + AS * X_BYTES + FIXED;
+  static constexpr int TOTAL = AS * A_BYTES + BS * B_BYTES + AS * X_BYTES + OUT_BYTES + MISC_BYTES;
   // TMEM accumulator buffers (the bf16 kinds keep columns 256.. for the
   // decoded-weight ring)
   static constexpr int NBUF = (BT > 128 || (KIND != KIND_F8F8 && BT == 128)) ? 2 : 4;
@@ -468,8 +463,6 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
   float* sWr = reinterpret_cast<float*>(misc + 1024 + 8192);      // [SSL][128] row scales
   // F8Q: [8][BT] token-group scales As(m, kb), slot = slice % 8
   float* sQs = reinterpret_cast<float*>(misc + 1024 + 4096);
-  // [1, 128] token-major: [2][WCH][BT] column-scale chunks
-  float* sWs = reinterpret_cast<float*>(misc + L::MISC_BYTES);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -754,30 +747,35 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       // tile's columns, and this warp stages each slice's BT column scales
       // Ws(n, kb) in the shared ring, four slices ahead
       if (EPI == EPI_NORMAL_COLW) {
-        // chunk c of the CTA's sequence goes to buffer c % 2: WCH slices x BT
-        // columns, [slice][column], columns past N read as 1
-        constexpr int NW = BT / 32, WCH = L::WCH;
-        uint32_t ic = 0;
+        constexpr int NW = BT / 32;
+        uint32_t is = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
           const Unit U = get_unit<EPI, BT>(p, u);
-          for (int kc = U.kb0; kc < U.kb1; kc += WCH, ++ic) {
-            const int cb = ic & 1;
-            if (!mbar_wait(&s_empty[cb], ((ic >> 1) & 1) ^ 1, wc)) goto ncol_done;
-            const int nk = min(WCH, U.kb1 - kc);
-            float* dst = sWs + cb * (WCH * BT);
-#pragma unroll 4
-            for (int i = 0; i < nk; ++i) {
-              float w[NW];
+          float rw[4][NW];
+          auto fetch = [&](int kb, float* w) {
 #pragma unroll
-              for (int j = 0; j < NW; ++j) {
-                const int n = U.n0 + lane + 32 * j;
-                w[j] = n < p.N ? __ldg(p.w_scale + static_cast<int64_t>(n) * p.sw0 + (kc + i) * p.sw1) : 1.f;
-              }
-#pragma unroll
-              for (int j = 0; j < NW; ++j) dst[i * BT + lane + 32 * j] = w[j];
+            for (int i = 0; i < NW; ++i) {
+              const int n = U.n0 + lane + 32 * i;
+              w[i] = n < p.N ? __ldg(p.w_scale + static_cast<int64_t>(n) * p.sw0 + kb * p.sw1) : 1.f;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_full[cb]);
+          };
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (U.kb0 + q < U.kb1) fetch(U.kb0 + q, rw[q]);
+          for (int kb = U.kb0; kb < U.kb1; kb += 4) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (kb + q < U.kb1) {
+                const int slot = is % SSL;
+                if (!mbar_wait(&s_empty[slot], ((is / SSL) & 1) ^ 1, wc)) goto ncol_done;
+#pragma unroll
+                for (int i = 0; i < NW; ++i) sAsc[slot * BT + lane + 32 * i] = rw[q][i];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_full[slot]);
+                ++is;
+                if (kb + q + 4 < U.kb1) fetch(kb + q + 4, rw[q]);
+              }
+            }
           }
         }
       ncol_done:;
@@ -1103,13 +1101,12 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           rw[q] = colw ? 1.f : __ldg(wrow + (kb + 4) * wk);
         }
         const uint32_t buf = au % NB;
-        // [1, 128]: the slice's place in its column-scale chunk
-        const int kc = (kb - U.kb0) % L::WCH;
-        if (colw && kc == 0 && !mbar_wait(&s_full[is & 1], (is >> 1) & 1, wc)) goto epin_done;
+        const int slot = is % SSL;
+        if (colw && !mbar_wait(&s_full[slot], (is / SSL) & 1, wc)) goto epin_done;
         if (!mbar_wait(&t_full[buf], (au / NB) & 1, wc)) goto epin_done;
         tc_fence_after();
         const float2 s2 = make_float2(sc, sc);
-        const float* wcol = sWs + ((is & 1) * L::WCH + kc) * BT + col0;
+        const float* wcol = sAsc + slot * BT + col0;
 #pragma unroll
         for (int c = 0; c < COLS / GRP; ++c) {
           if (c < ngr) {
@@ -1151,9 +1148,9 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&t_empty[buf]);
         }
-        if (colw && (kc == L::WCH - 1 || kb + 1 == U.kb1)) {
+        if (colw) {
           __syncwarp();
-          if (lane == 0) mbar_arrive(&s_empty[is & 1]);
+          if (lane == 0) mbar_arrive(&s_empty[slot]);
           ++is;
         }
         ++au;

@@ -236,6 +236,10 @@ def test_full_size_block1x128_sampled_rows(oracle, M):
     rf, rb = oracle.scaled_mm(rq, E4M3, rs, u8(wq), ws.cpu().numpy(), 1, 128)
     assert_bf16_close(flat[ridx], rb)
     assert_probe_close(o32[ridx], rf)
+    if M > 128:
+        # token-major tiles, scales stored [kb][n]: the same bits
+        t32 = mxq.fp8_scaled_mm(q, wq, transposed(ws), [1, 128], a_scale=s, out_dtype=torch.float32)
+        assert torch.equal(t32, o32)
 
 
 @pytest.mark.parametrize("tile", [128, 192, 256])
@@ -262,13 +266,29 @@ def test_per_row_weight_scales_large_m(oracle, seed):
                bias=torch.randn(200, generator=torch.Generator().manual_seed(seed)))
 
 
+def transposed(t):
+    """The same values stored column-major ([kb][n] in memory)."""
+    out = torch.empty_strided(t.shape, (1, t.shape[0]), dtype=t.dtype, device=t.device)
+    out.copy_(t)
+    return out
+
+
 @pytest.mark.parametrize("M,N,K", [(260, 392, 2400), (140, 136, 4224)])
-def test_per_row_weight_scales_chunk_tails(oracle, M, N, K):
+def test_per_row_weight_scales_long_k_both_layouts(oracle, M, N, K):
     """[1,128] weight scales on the token-major tiles with K slice counts of
-    19 and 33: the column scales are staged in chunks of 16 slices, so both
-    shapes end on a partial chunk (the first with a ragged K tail as well)."""
-    block_case(oracle, M, N, K, 1, seed=M + K,
-               bias=torch.randn(N, generator=torch.Generator().manual_seed(K)))
+    19 (a ragged K tail) and 33, more than the scale ring's eight slots; scales
+    stored [n][kb] and [kb][n] give the same bits."""
+    bias = torch.randn(N, generator=torch.Generator().manual_seed(K))
+    o32, o16 = block_case(oracle, M, N, K, 1, seed=M + K, bias=bias)
+    x = synth.activations(M, K, seed=M + K).cuda()
+    wq, ws = synth.block_fp8_weight(N, K, 1, seed=M + K + 1)
+    q, s = mxq.per_token_group_quant_fp8(x)
+    wst = transposed(ws.cuda())
+    t32 = mxq.fp8_scaled_mm(q, wq.cuda(), wst, [1, 128], a_scale=s, bias=bias.cuda(),
+                            out_dtype=torch.float32)
+    t16 = mxq.fp8_scaled_mm(q, wq.cuda(), wst, [1, 128], a_scale=s, bias=bias.cuda())
+    mxq.sync_status()
+    assert torch.equal(t32, o32) and torch.equal(t16, o16)
 
 
 @pytest.mark.parametrize("tile", [32, 64, 128, 256])
