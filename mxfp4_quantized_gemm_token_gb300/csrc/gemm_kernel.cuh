@@ -1083,23 +1083,48 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
       const int wb = min((U.n0 + col0) / 128, (p.N - 1) / 128);
       const float* wrow = p.w_scale + (p.block_n != 128 ? 0 : static_cast<int64_t>(wb) * p.sw0);
       const int64_t wk = p.block_n != 128 ? 0 : p.sw1;
-      float ra[4], rw[4];
+      // four slices' scales at a time, with one 16-byte load where the layout
+      // allows it (a thread's As row and the block's Ws row contiguous and
+      // aligned); the next four are loaded while these are used
+      const bool va = p.sa1 == 1 && (p.sa0 & 3) == 0 && (U.kb0 & 3) == 0 &&
+                      (reinterpret_cast<uintptr_t>(p.a_scale) & 15) == 0;
+      const bool vw = !colw && wk == 1 && ((static_cast<int64_t>(wb) * p.sw0) & 3) == 0 &&
+                      (U.kb0 & 3) == 0 && (reinterpret_cast<uintptr_t>(p.w_scale) & 15) == 0;
+      auto scales4 = [&](int kb, float* a, float* w) {
+        if (va && kb + 4 <= U.kb1) {
+          const float4 t = __ldg(reinterpret_cast<const float4*>(arow + kb));
+          a[0] = t.x;
+          a[1] = t.y;
+          a[2] = t.z;
+          a[3] = t.w;
+        } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int k = min(U.kb0 + q, U.kb1 - 1);
-        ra[q] = __ldg(arow + k * p.sa1);
-        rw[q] = colw ? 1.f : __ldg(wrow + k * wk);
-      }
-      for (int kb4 = U.kb0; kb4 < U.kb1; kb4 += 4)
+          for (int q = 0; q < 4; ++q) a[q] = __ldg(arow + min(kb + q, U.kb1 - 1) * p.sa1);
+        }
+        if (colw) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) w[q] = 1.f;
+        } else if (vw && kb + 4 <= U.kb1) {
+          const float4 t = __ldg(reinterpret_cast<const float4*>(wrow + kb));
+          w[0] = t.x;
+          w[1] = t.y;
+          w[2] = t.z;
+          w[3] = t.w;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) w[q] = __ldg(wrow + min(kb + q, U.kb1 - 1) * wk);
+        }
+      };
+      float ra[4], rw[4];
+      scales4(U.kb0, ra, rw);
+      for (int kb4 = U.kb0; kb4 < U.kb1; kb4 += 4) {
+      float na[4] = {0.f, 0.f, 0.f, 0.f}, nw[4] = {0.f, 0.f, 0.f, 0.f};
+      if (kb4 + 4 < U.kb1) scales4(kb4 + 4, na, nw);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int kb = kb4 + q;
         if (kb >= U.kb1) break;
         const float sc = ra[q] * rw[q];
-        if (kb + 4 < U.kb1) {
-          ra[q] = __ldg(arow + (kb + 4) * p.sa1);
-          rw[q] = colw ? 1.f : __ldg(wrow + (kb + 4) * wk);
-        }
         const uint32_t buf = au % NB;
         const int slot = is % SSL;
         if (colw && !mbar_wait(&s_full[slot], (is / SSL) & 1, wc)) goto epin_done;
@@ -1154,6 +1179,12 @@ __global__ void __launch_bounds__(Layout<KIND, BT, EPI>::kThreads, 1)
           ++is;
         }
         ++au;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        ra[q] = na[q];
+        rw[q] = nw[q];
+      }
       }
       // ------------------------------------------------------- output
       if (mrow && colv > 0) {
