@@ -37,7 +37,7 @@ N_W, K_W = 18432, 7168
 #  -k regex:gemm_kernel -s 1 -c 1 python bench.py --profile 4096`
 # (summarised in profiles/); set to None whenever that kernel changes.
 DOMINANT_KERNEL = "gemm_kernel<F8F8, NORMAL, 128, promote> (M=4096)"
-DOMINANT_TRAFFIC_BYTES = 163.284992e6 + 127.012864e6
+DOMINANT_TRAFFIC_BYTES = 164.238848e6 + 125.967360e6
 M_SET = (1, 8, 17, 128, 1024, 4096)
 METRIC = "FP8 block-scaled W8A8 linear (quant + scaled GEMM) throughput, [128,128] weights"
 WORKLOAD = ("block-FP8 W8A8 linear, W e4m3 [18432, 7168] with [128,128] fp32 block scales, "
