@@ -69,3 +69,29 @@ def test_quant_full_size_block_workload_sampled_rows(oracle):
     rq, rs = oracle.per_token_group_quant_fp8(bits16(x[ridx]), 128)
     assert np.array_equal(u8(q[ridx]), rq)
     assert np.array_equal(s[ridx].cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+def every_bf16_below(amax, binades=14):
+    """All bf16 magnitudes from amax * 2^-binades up to amax, with both signs."""
+    top = int(torch.tensor([amax], dtype=torch.bfloat16).view(torch.int16).item())
+    lo = top - binades * 128
+    mags = torch.arange(max(lo, 1), top + 1, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    return torch.cat([mags, -mags])
+
+
+@pytest.mark.parametrize("amax", [1.0, 3.0, 5.0, 7.0, 0.3, 123.0, 1e-3, 2.5e4, 448.0, 1e-20])
+def test_quant_every_bf16_input_per_scale(oracle, amax):
+    """Every bf16 value within 2^14 of the group's largest, for scales s =
+    amax / 448 that are and are not powers of two: the quotients x / s fall
+    on, near and between all e4m3 rounding midpoints (and in the e4m3
+    subnormal range), so any code reached by a route other than the IEEE
+    division that disagrees with it shows up here."""
+    vals = every_bf16_below(amax)
+    a = torch.tensor([amax], dtype=torch.bfloat16)
+    n = (vals.numel() + 126) // 127
+    pad = torch.zeros(n * 127 - vals.numel(), dtype=torch.bfloat16)
+    body = torch.cat([vals, pad]).view(n, 127)
+    groups = torch.cat([a.expand(n, 1), body], dim=1)          # each group's largest is amax
+    rows = (n + 7) // 8
+    x = torch.cat([groups, torch.zeros(rows * 8 - n, 128, dtype=torch.bfloat16)]).view(rows, 8 * 128)
+    check(oracle, x)
