@@ -276,13 +276,23 @@ __device__ __forceinline__ unsigned row_max_u8(const uint8_t* row, int ncols, in
   return m;
 }
 
+// rows of at most EMAX_STAGE_COLS bytes, stored back to back (ld == ncols)
+// and 16-byte aligned per chunk: a chunk of 256 rows is one contiguous range,
+// read with coalesced 16-byte loads into shared memory, and each thread then
+// takes its row's maximum there (a thread reading its own row from global
+// memory touches a separate line per lane)
+constexpr int EMAX_STAGE_COLS = 160;
+
 __global__ void __launch_bounds__(256) mx_row_emax_kernel(
     const uint8_t* __restrict__ s1, int64_t rows1, int ncols1, int64_t ld1, uint8_t* __restrict__ e1,
     const uint8_t* __restrict__ s2, int64_t rows2, int ncols2, int64_t ld2, uint8_t* __restrict__ e2,
-    int align, const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ num_blocks,
-    int E, int64_t ch1, int64_t ch2) {
+    int align, int staged, const int32_t* __restrict__ expert_ids,
+    const int32_t* __restrict__ num_blocks, int E, int64_t ch1, int64_t ch2) {
+  __shared__ __align__(16) uint8_t sbuf[256 * EMAX_STAGE_COLS];
   pdl_wait();
   pdl_launch_dependents();
+  // every exit below depends on the block index only, so the whole CTA
+  // leaves together and the barriers of the staged path are uniform
   const int b = blockIdx.x;
   if (b >= __ldg(num_blocks)) return;
   const int e = __ldg(expert_ids + b);
@@ -290,13 +300,33 @@ __global__ void __launch_bounds__(256) mx_row_emax_kernel(
   for (int64_t c = blockIdx.y; c < ch1 + ch2; c += gridDim.y) {
     const bool second = c >= ch1;
     const int64_t rows = second ? rows2 : rows1;
-    const int64_t r = (second ? c - ch1 : c) * 256 + threadIdx.x;
-    if (r >= rows) continue;
+    const int64_t r0 = (second ? c - ch1 : c) * 256;
     const uint8_t* base = second ? s2 : s1;
     const int64_t ld = second ? ld2 : ld1;
-    const unsigned m = row_max_u8(base + (static_cast<int64_t>(e) * rows + r) * ld,
-                                  second ? ncols2 : ncols1, align);
-    (second ? e2 : e1)[static_cast<int64_t>(e) * rows + r] = static_cast<uint8_t>(m);
+    const int ncols = second ? ncols2 : ncols1;
+    uint8_t* out = (second ? e2 : e1) + static_cast<int64_t>(e) * rows + r0;
+    if (staged) {
+      const int nr = static_cast<int>(rows - r0 < 256 ? rows - r0 : 256);
+      const int nbytes = nr * ncols;
+      const uint8_t* src = base + (static_cast<int64_t>(e) * rows + r0) * ld;
+      __syncthreads();   // the previous chunk's rows have been read
+      for (int i = threadIdx.x; i < nbytes / 16; i += 256)
+        reinterpret_cast<uint4*>(sbuf)[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+      for (int i = (nbytes / 16) * 16 + threadIdx.x; i < nbytes; i += 256) sbuf[i] = __ldg(src + i);
+      __syncthreads();
+      if (static_cast<int>(threadIdx.x) < nr) {
+        const uint8_t* row = sbuf + threadIdx.x * ncols;
+        unsigned m = 0;
+#pragma unroll 8
+        for (int j = 0; j < ncols; ++j) m = max(m, static_cast<unsigned>(row[j]));
+        out[threadIdx.x] = static_cast<uint8_t>(m);
+      }
+    } else {
+      const int64_t r = r0 + threadIdx.x;
+      if (r >= rows) continue;
+      out[threadIdx.x] = static_cast<uint8_t>(
+          row_max_u8(base + (static_cast<int64_t>(e) * rows + r) * ld, ncols, align));
+    }
   }
 }
 
@@ -310,13 +340,19 @@ cudaError_t launch_mx_row_emax(const void* s1, int64_t rows1, int64_t ncols1, in
   const uintptr_t a = reinterpret_cast<uintptr_t>(s1) | reinterpret_cast<uintptr_t>(s2) |
                       static_cast<uintptr_t>(ld1) | static_cast<uintptr_t>(ld2);
   const int align = (a & 3) == 0 ? 4 : ((a & 1) == 0 ? 2 : 1);
+  // staged: rows back to back, short enough for the shared buffer, and every
+  // chunk of 256 rows of every expert starting on a 16-byte boundary
+  const int staged = ld1 == ncols1 && ld2 == ncols2 && ncols1 <= EMAX_STAGE_COLS &&
+                     ncols2 <= EMAX_STAGE_COLS &&
+                     ((reinterpret_cast<uintptr_t>(s1) | reinterpret_cast<uintptr_t>(s2)) & 15) == 0 &&
+                     (rows1 * ld1) % 16 == 0 && (rows2 * ld2) % 16 == 0;
   const int64_t ch1 = (rows1 + 255) / 256, ch2 = (rows2 + 255) / 256;
   const unsigned gy = static_cast<unsigned>(std::min<int64_t>(ch1 + ch2, 65535));
   return launch_k(mx_row_emax_kernel, dim3(static_cast<unsigned>(cap), gy), dim3(256), 0, stream,
                   reinterpret_cast<const uint8_t*>(s1), rows1, static_cast<int>(ncols1), ld1,
                   reinterpret_cast<uint8_t*>(e1), reinterpret_cast<const uint8_t*>(s2), rows2,
-                  static_cast<int>(ncols2), ld2, reinterpret_cast<uint8_t*>(e2), align, expert_ids,
-                  num_blocks, E, ch1, ch2);
+                  static_cast<int>(ncols2), ld2, reinterpret_cast<uint8_t*>(e2), align, staged,
+                  expert_ids, num_blocks, E, ch1, ch2);
 }
 
 // ------------------------------------------------------------ row gather
